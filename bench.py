@@ -1,0 +1,317 @@
+"""Benchmark of the Muse Glimmer decode output stage on GB300.
+
+One step = one forward of the whole output stage (final RMSNorm, Q5_K LM-head
+matvec, scale, soft cap, argmax) over one batch of synthetic input.  Default
+workload: the full LM head, batch 1 (202,048 x 6,656 Q5_K weights, ~925 MB,
+rows 0/777/200001 boosted so the cap bites).
+
+Prints ONE JSON line (rank 0).  `value` is the achieved algorithmic bandwidth
+(Q5_K weights + hidden + gamma + logits bytes per forward / device time per
+forward), GB/s, with inputs resident in HBM.  Extra keys: us_per_forward,
+logits_per_s, roofline (dominant kernel vs the measured HBM copy peak),
+cpu_baseline (the f64 oracle on this host's cores, a bounded row sample), e2e
+(the same metric through the host-buffer C-ABI call, copies included), clocks
+sampled during the timed region, gpu_launches.
+
+--impl reference times the oracle (the reference implementation of this
+build) on the host cores, as it stands, on the same workload and metric.
+
+Multi-GPU: the stage does not shard in this deployment; --gpus N runs N
+independent replicas (one per rank), value = all ranks' bytes / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 126 * 1024 * 1024   # GB300 L2 (per nvidia-smi/cudaDeviceProp order of magnitude)
+
+
+def _measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background (200 ms period)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _oracle_rate(wl, hidden, gamma, wq, target_s: float):
+    """Time the oracle on a bounded row sample; returns (bytes_per_s, rows, cores, secs)."""
+    import numpy as np
+    import oracle
+    cores = oracle.default_threads()
+    rows_per_block = 2048
+    t0 = time.perf_counter()
+    oracle.lmhead(hidden, gamma, wq[:rows_per_block], wl.scale, wl.cap, nthreads=cores)
+    dt = time.perf_counter() - t0
+    rows = int(min(wl.n_rows, max(rows_per_block, rows_per_block * target_s / max(dt, 1e-6))))
+    sample = np.ascontiguousarray(wq[:rows])
+    t0 = time.perf_counter()
+    oracle.lmhead(hidden, gamma, sample, wl.scale, wl.cap, nthreads=cores)
+    secs = time.perf_counter() - t0
+    frac = rows / wl.n_rows
+    bytes_sample = wl.algorithmic_bytes() * frac
+    return bytes_sample / secs, rows, cores, secs
+
+
+def run_reference(args, wl):
+    """The oracle (f64 CPU) as the reference arm."""
+    import q5k_synth as synth
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    hidden, gamma, wq = synth.inputs_for(wl)
+    per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        _oracle_rate(wl, hidden, gamma, wq, per_step * 0.2)
+    rates, rows_l, secs_l, cores = [], [], [], 1
+    for _ in range(args.steps):
+        r, rows, cores, secs = _oracle_rate(wl, hidden, gamma, wq, per_step)
+        rates.append(r)
+        rows_l.append(rows)
+        secs_l.append(secs)
+    value = statistics.median(rates) / 1e9
+    sample = f"{int(statistics.median(rows_l))} of {wl.n_rows} rows x batch {wl.batch} per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(statistics.median(secs_l) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(wl, 1, "cpu"),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "Q5_K LM-head forward us and achieved HBM GB/s (% of GB300 peak), batch 1-32"
+
+
+def _config(wl, ws, l2_mode):
+    return {"workload": wl.name, "n_rows": wl.n_rows, "k": wl.k, "batch": wl.batch,
+            "weights": "Q5_K 176 B / 256 weights", "final_norm": wl.norm, "scale": wl.scale, "cap": wl.cap,
+            "argmax": wl.argmax, "l2": l2_mode, "parallelism": f"replicas x{ws}"}
+
+
+def run_ours(args, wl):
+    import numpy as np
+    import torch
+    import q5k_synth as synth
+    import q5_lm_head_gb300 as mlh
+    from q5_lm_head_gb300 import _build
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(mlh.LIB_PATH):
+        _build.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    mlh.load_library()
+
+    hidden, gamma, wq = synth.inputs_for(wl)
+    h_d = torch.from_numpy(hidden).to(dev)
+    g_d = None if gamma is None else torch.from_numpy(gamma).to(dev)
+    w_d = torch.from_numpy(wq).to(dev)
+    head = mlh.LMHead(wl.n_rows, wl.k, max_batch=wl.batch, device=local)
+    logits = torch.empty((wl.batch, wl.n_rows), dtype=torch.float32, device=dev)
+    amax = torch.empty((wl.batch,), dtype=torch.int32, device=dev) if wl.argmax else None
+    stream = torch.cuda.Stream(dev)
+    eps = synth.RMS_EPS
+    big = wl.algorithmic_bytes() > 2 * L2_BYTES
+    l2_mode = ("inputs larger than L2 (weights stream from HBM every forward)" if big else
+               "L2 flushed before every timed forward (256 MiB write, outside the timed interval)")
+    flush = None if big else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        head.forward(h_d, w_d, g_d, eps, wl.scale, wl.cap, wl.argmax, logits, amax, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            fwd()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_begin.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            fwd()
+            ends[i].record(stream)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]     # ms, each forward
+    kern_ms = sum(per) / len(per)
+    wall_ms = t_begin.elapsed_time(t_end)
+    step_ms = kern_ms if flush is not None else wall_ms / args.steps
+    if ws > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    nbytes = wl.algorithmic_bytes()
+    value = ws * nbytes / (step_ms * 1e-3) / 1e9
+    status = head.device_status()
+
+    # end to end through the host-buffer entry point: pinned hidden in, logits + argmax out
+    h_pin = torch.from_numpy(hidden).pin_memory()
+    l_pin = torch.empty((wl.batch, wl.n_rows), dtype=torch.float32, pin_memory=True)
+    a_pin = torch.empty((wl.batch,), dtype=torch.int32, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        head.forward_host(h_pin, w_d, g_d, eps, wl.scale, wl.cap, l_pin, a_pin if wl.argmax else None, stream)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        head.forward_host(h_pin, w_d, g_d, eps, wl.scale, wl.cap, l_pin, a_pin if wl.argmax else None, stream)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    h2d = wl.batch * wl.k * 4
+    d2h = wl.batch * wl.n_rows * 4 + (wl.batch * 4 if wl.argmax else 0)
+
+    peak, peak_kind = _measured_peaks()
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded Q5_K weights and N(0,1) hidden rows; no checkpoint)",
+        "config": _config(wl, ws, l2_mode),
+        "us_per_forward": round(step_ms * 1e3, 2),
+        "logits_per_s": round(ws * wl.batch * wl.n_rows / (step_ms * 1e-3), 1),
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "kernel_path": head.path_name(wl.batch),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "kernel": head.path_name(wl.batch),
+                     "algorithmic_bytes_per_launch": nbytes if head.launches_per_forward(wl.batch, wl.norm) == 1 else None},
+        "e2e": {"value": round(ws * nbytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "us_per_forward": round(e2e_s * 1e6, 2)},
+        "gpu_launches": head.launches_per_forward(wl.batch, wl.norm) * args.steps,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, rows, cores, secs = _oracle_rate(wl, hidden, gamma, wq, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(rate / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{rows} of {wl.n_rows} weight rows x batch {wl.batch} "
+                                          f"({secs:.1f} s wall on {cores} threads)"}
+    head.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    import q5k_synth as synth
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="lmhead_b1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

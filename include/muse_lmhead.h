@@ -1,0 +1,139 @@
+/*
+ * muse_lmhead — decode-time output stage of the 52-layer Muse Glimmer model on
+ * one GB300 (sm_103a): final RMSNorm -> Q5_K LM-head matvec -> logit scale ->
+ * soft cap -> optional greedy argmax, as one asynchronous call.
+ *
+ * What the operation is ("Chapter 20 — Final norm, LM head, and the soft cap",
+ * §20.1; the order scale-then-cap is also fixed by "Chapter 9 — The Muse
+ * Glimmer architecture", §9.10), for every batch row b and weight row i:
+ *
+ *     r_b      = 1 / sqrt( sum_j hidden[b][j]^2 / k + eps )        (final norm)
+ *     x[b][j]  = hidden[b][j] * r_b * gamma[j]
+ *     raw[b][i]= sum_j W[i][j] * x[b][j]                            (LM head)
+ *     v        = raw[b][i] * scale                                   (logit_scale)
+ *     logits[b][i] = cap > 0 ? cap * tanh(v / cap) : v               (soft cap)
+ *     argmax[b]    = lowest i with the largest logits[b][i]          (greedy pick)
+ *
+ * W is [n_rows x k] in Q5_K super-blocks (§20.3: 256 weights per 176 bytes,
+ * k/256 blocks per row, rows contiguous): fp16 d, fp16 dmin, 12 bytes of 6-bit
+ * sub-block scales/mins, 32 bytes of high bits, 128 bytes of low nibbles, with
+ * w = d*sc*q - dmin*m (the ggml block_q5_K layout).
+ *
+ * Conventions for every call:
+ *   - Device pointers are global-memory addresses on the handle's device.  The
+ *     caller owns every input and output buffer; the library never frees them.
+ *   - Layouts are dense row-major: hidden [batch][k] f32, gamma [k] f32,
+ *     weights [n_rows][k/256][176] bytes, logits [batch][n_rows] f32,
+ *     argmax [batch] int32.
+ *   - hidden, gamma, weights and logits must be 16-byte aligned; argmax 4-byte.
+ *   - Every call validates its arguments first and fails closed: on any error it
+ *     returns a negative status and launches nothing.  Nothing aborts, traps or
+ *     prints.  Asynchronous device faults surface on the caller's next
+ *     synchronisation, as usual in CUDA.
+ *   - A handle keeps a small device workspace (argmax partial keys and a
+ *     completion counter, and split-K partial sums for short matrices).  Two
+ *     forwards that may run at the same time on the GPU must use two handles.
+ */
+#ifndef MUSE_LMHEAD_H
+#define MUSE_LMHEAD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define MUSE_OK 0
+#define MUSE_ERR_NULL (-1)      /* a required pointer is NULL */
+#define MUSE_ERR_SHAPE (-2)     /* n_rows < 1, k < 256, k % 256 != 0, or too large */
+#define MUSE_ERR_BATCH (-3)     /* batch outside 1..max_batch, or max_batch outside 1..32 */
+#define MUSE_ERR_ALIGN (-4)     /* a pointer is not aligned as stated above */
+#define MUSE_ERR_VALUE (-5)     /* eps < 0 or not finite, scale or cap not finite */
+#define MUSE_ERR_DEVICE (-6)    /* bad device index, or not an sm_103 GPU */
+#define MUSE_ERR_CUDA (-7)      /* a CUDA runtime call failed (message via status_string) */
+#define MUSE_ERR_NOMEM (-8)     /* workspace or host allocation failed */
+
+/* Largest batch a handle can be created for. */
+#define MUSE_MAX_BATCH 32
+
+typedef struct muse_lmhead muse_lmhead;
+
+/*
+ * Create a handle for an [n_rows x k] Q5_K weight matrix and batches of up to
+ * max_batch rows on CUDA device `device`.  Allocates the handle's device
+ * workspace (zeroed) on that device.  *out receives the handle, or NULL on
+ * error.  Returns MUSE_OK or a negative status.
+ * The shapes of the pages: n_rows = 202,048 (vocabulary), k = 6,656 (hidden
+ * width), Chapter 20 §20.3.
+ */
+int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k,
+                     int max_batch);
+
+/*
+ * One forward on `stream` (a cudaStream_t; NULL = the legacy default stream),
+ * asynchronous with respect to the host.
+ *   hidden  [batch][k] f32, device.  The residual stream after the last layer.
+ *   gamma   [k] f32, device, or NULL to skip the final norm (then x = hidden).
+ *   eps     RMSNorm epsilon (1e-5 on the pages); ignored when gamma is NULL.
+ *   weights Q5_K blocks, device, n_rows * (k/256) * 176 bytes.
+ *   scale   logit scale (0.196116 on the pages).
+ *   cap     soft cap (20 on the pages); cap <= 0 turns the cap off.
+ *   logits  [batch][n_rows] f32, device, written.
+ *   argmax  [batch] int32, device, written; or NULL to skip the argmax.
+ * hidden/gamma/weights are only read; logits must not overlap them.
+ */
+int muse_lmhead_forward(muse_lmhead *h, const float *hidden, int batch,
+                        const float *gamma, float eps, const void *weights,
+                        float scale, float cap, float *logits, int32_t *argmax,
+                        void *stream);
+
+/*
+ * The same forward for callers whose activations live in host memory: copies
+ * hidden_host to the device, runs the forward, copies the logits (and argmax)
+ * back, and waits for `stream` before returning.  gamma and weights are device
+ * pointers (they stay resident).  logits_host may be NULL to fetch only the
+ * argmax; argmax_host may be NULL to skip it.  Host buffers should be pinned
+ * (page-locked) for full copy bandwidth; pageable memory also works.  The first
+ * call allocates the handle's device staging buffers (max_batch rows).
+ */
+int muse_lmhead_forward_host(muse_lmhead *h, const float *hidden_host, int batch,
+                             const float *gamma, float eps, const void *weights,
+                             float scale, float cap, float *logits_host,
+                             int32_t *argmax_host, void *stream);
+
+/*
+ * Number of kernel launches one forward issues for this batch size, with
+ * (with_norm != 0) or without the final norm, or a negative status.  Host-only
+ * query.
+ */
+int muse_lmhead_launches_per_forward(const muse_lmhead *h, int batch, int with_norm);
+
+/*
+ * Name of the kernel path a forward with this batch size takes ("gemv_b1",
+ * "gemv_generic", ...), or NULL for an invalid handle/batch.  Host-only query;
+ * the string is static.
+ */
+const char *muse_lmhead_path_name(const muse_lmhead *h, int batch);
+
+/*
+ * Read the handle's sticky device status word (synchronous device-to-host copy
+ * on the legacy default stream, after all prior work on the device).  Bit 0:
+ * a kernel's bounded wait for a pipeline stage gave up (the forward's outputs
+ * are then invalid).  0 means no fault has been recorded since init.
+ */
+int muse_lmhead_device_status(muse_lmhead *h, uint32_t *status_out);
+
+/* Free the handle and its workspace.  NULL is allowed.  Must not be called
+ * while a forward using the handle may still be running on the GPU. */
+void muse_lmhead_destroy(muse_lmhead *h);
+
+/* Static English text for a status code; for MUSE_ERR_CUDA it names the last
+ * CUDA error seen by this thread's failing call. */
+const char *muse_lmhead_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUSE_LMHEAD_H */

@@ -1,0 +1,229 @@
+"""Python binding of libmuse_lmhead.so: the Muse Glimmer decode output stage
+(final RMSNorm -> Q5_K LM-head matvec -> scale -> soft cap -> argmax) on one
+GB300.
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels.  PyTorch supplies device memory and streams.  The functions named
+``muse_lmhead_*`` mirror the C-ABI in include/muse_lmhead.h one to one (plain
+integers for pointers and streams); :class:`LMHead` wraps them for torch
+tensors.  If the compiled library is missing, importing works but every call
+raises: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "LMHead", "MuseError", "library_path", "load_library",
+    "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
+    "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
+    "muse_lmhead_destroy", "muse_lmhead_status_string", "EXPORTED_SYMBOLS",
+    "LOGIT_SCALE", "SOFTCAP", "RMS_EPS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmuse_lmhead.so")
+
+# Constants of the Muse Glimmer checkpoint ("Chapter 20 — Final norm, LM head,
+# and the soft cap", §20.1 and §20.5): read from GGUF metadata there, passed as
+# call arguments here.
+LOGIT_SCALE = 0.196116
+SOFTCAP = 20.0
+RMS_EPS = 1e-5
+
+EXPORTED_SYMBOLS = (
+    "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
+    "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
+    "muse_lmhead_destroy", "muse_lmhead_status_string",
+)
+
+MUSE_OK = 0
+MUSE_MAX_BATCH = 32
+STATUS_WAIT_TIMEOUT = 1
+
+_lib = None
+
+
+class MuseError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {muse_lmhead_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library():
+    """Load the compiled library; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"libmuse_lmhead.so is not built ({LIB_PATH}); run `python -c \"import __graft_entry__ as g; "
+            "g.build()\"` or `python q5_lm_head_gb300/_build.py`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    lib.muse_lmhead_init.restype = i32
+    lib.muse_lmhead_init.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i32]
+    lib.muse_lmhead_forward.restype = i32
+    lib.muse_lmhead_forward.argtypes = [vp, vp, i32, vp, f32, vp, f32, f32, vp, vp, vp]
+    lib.muse_lmhead_forward_host.restype = i32
+    lib.muse_lmhead_forward_host.argtypes = [vp, vp, i32, vp, f32, vp, f32, f32, vp, vp, vp]
+    lib.muse_lmhead_launches_per_forward.restype = i32
+    lib.muse_lmhead_launches_per_forward.argtypes = [vp, i32, i32]
+    lib.muse_lmhead_path_name.restype = ctypes.c_char_p
+    lib.muse_lmhead_path_name.argtypes = [vp, i32]
+    lib.muse_lmhead_device_status.restype = i32
+    lib.muse_lmhead_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.muse_lmhead_destroy.restype = None
+    lib.muse_lmhead_destroy.argtypes = [vp]
+    lib.muse_lmhead_status_string.restype = ctypes.c_char_p
+    lib.muse_lmhead_status_string.argtypes = [i32]
+    _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------ same-named C-ABI calls
+def muse_lmhead_init(device: int, n_rows: int, k: int, max_batch: int) -> int:
+    """Returns the handle (an integer) or raises MuseError."""
+    h = ctypes.c_void_p()
+    st = load_library().muse_lmhead_init(ctypes.byref(h), device, n_rows, k, max_batch)
+    if st != MUSE_OK:
+        raise MuseError(st, "muse_lmhead_init")
+    return h.value
+
+
+def muse_lmhead_forward(h: int, hidden: int, batch: int, gamma: int | None, eps: float, weights: int,
+                        scale: float, cap: float, logits: int, argmax: int | None, stream: int | None) -> int:
+    return load_library().muse_lmhead_forward(h, hidden, batch, gamma, eps, weights, scale, cap, logits,
+                                              argmax, stream)
+
+
+def muse_lmhead_forward_host(h: int, hidden_host: int, batch: int, gamma: int | None, eps: float,
+                             weights: int, scale: float, cap: float, logits_host: int | None,
+                             argmax_host: int | None, stream: int | None) -> int:
+    return load_library().muse_lmhead_forward_host(h, hidden_host, batch, gamma, eps, weights, scale, cap,
+                                                   logits_host, argmax_host, stream)
+
+
+def muse_lmhead_launches_per_forward(h: int, batch: int, with_norm: bool) -> int:
+    return load_library().muse_lmhead_launches_per_forward(h, batch, int(bool(with_norm)))
+
+
+def muse_lmhead_path_name(h: int, batch: int) -> str | None:
+    r = load_library().muse_lmhead_path_name(h, batch)
+    return None if r is None else r.decode()
+
+
+def muse_lmhead_device_status(h: int) -> int:
+    v = ctypes.c_uint32()
+    st = load_library().muse_lmhead_device_status(h, ctypes.byref(v))
+    if st != MUSE_OK:
+        raise MuseError(st, "muse_lmhead_device_status")
+    return v.value
+
+
+def muse_lmhead_destroy(h: int | None) -> None:
+    if h:
+        load_library().muse_lmhead_destroy(h)
+
+
+def muse_lmhead_status_string(status: int) -> str:
+    return load_library().muse_lmhead_status_string(status).decode()
+
+
+# ------------------------------------------------------------ torch-facing wrapper
+class LMHead:
+    """A handle for one [n_rows x k] Q5_K matrix and batches up to max_batch."""
+
+    def __init__(self, n_rows: int, k: int, max_batch: int = MUSE_MAX_BATCH, device: int | None = None):
+        import torch
+        self.device = torch.cuda.current_device() if device is None else int(device)
+        self.n_rows, self.k, self.max_batch = int(n_rows), int(k), int(max_batch)
+        self.handle = muse_lmhead_init(self.device, self.n_rows, self.k, self.max_batch)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            muse_lmhead_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def _check(self, t, name, dtype, shape=None):
+        import torch
+        if t.dtype != dtype or not t.is_contiguous() or t.device.type != "cuda" or t.device.index != self.device:
+            raise ValueError(f"{name}: need a contiguous {dtype} tensor on cuda:{self.device}")
+        if shape is not None and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+        return t.data_ptr()
+
+    def forward(self, hidden, weights, gamma=None, eps: float = RMS_EPS, scale: float = LOGIT_SCALE,
+                cap: float = SOFTCAP, want_argmax: bool = True, logits=None, argmax=None, stream=None):
+        """logits [B, n_rows] f32 (and argmax [B] int32) for hidden [B, k] f32 on the GPU."""
+        import torch
+        if hidden.dim() == 1:
+            hidden = hidden.unsqueeze(0)
+        b = hidden.shape[0]
+        hp = self._check(hidden, "hidden", torch.float32, (b, self.k))
+        wp = self._check(weights, "weights", torch.uint8)
+        if weights.numel() != self.n_rows * (self.k // 256) * 176:
+            raise ValueError("weights: wrong number of bytes for this handle")
+        gp = None if gamma is None else self._check(gamma, "gamma", torch.float32, (self.k,))
+        if logits is None:
+            logits = torch.empty((b, self.n_rows), dtype=torch.float32, device=hidden.device)
+        lp = self._check(logits, "logits", torch.float32, (b, self.n_rows))
+        ap = None
+        if want_argmax:
+            if argmax is None:
+                argmax = torch.empty((b,), dtype=torch.int32, device=hidden.device)
+            ap = self._check(argmax, "argmax", torch.int32, (b,))
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        st = muse_lmhead_forward(self.handle, hp, b, gp, float(eps), wp, float(scale), float(cap), lp, ap,
+                                 s.cuda_stream)
+        if st != MUSE_OK:
+            raise MuseError(st, "muse_lmhead_forward")
+        return (logits, argmax) if want_argmax else logits
+
+    def forward_host(self, hidden_host, weights, gamma=None, eps: float = RMS_EPS, scale: float = LOGIT_SCALE,
+                     cap: float = SOFTCAP, logits_host=None, argmax_host=None, stream=None):
+        """Host-memory forward: hidden_host [B, k] f32 CPU tensor (pinned for speed); returns CPU tensors."""
+        import torch
+        if hidden_host.dim() == 1:
+            hidden_host = hidden_host.unsqueeze(0)
+        if hidden_host.device.type != "cpu" or hidden_host.dtype != torch.float32 or not hidden_host.is_contiguous():
+            raise ValueError("hidden_host: need a contiguous f32 CPU tensor")
+        b = hidden_host.shape[0]
+        if logits_host is None:
+            logits_host = torch.empty((b, self.n_rows), dtype=torch.float32, pin_memory=True)
+        if argmax_host is None:
+            argmax_host = torch.empty((b,), dtype=torch.int32, pin_memory=True)
+        wp = self._check(weights, "weights", torch.uint8)
+        gp = None if gamma is None else self._check(gamma, "gamma", torch.float32, (self.k,))
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        st = muse_lmhead_forward_host(self.handle, hidden_host.data_ptr(), b, gp, float(eps), wp, float(scale),
+                                      float(cap), logits_host.data_ptr(), argmax_host.data_ptr(), s.cuda_stream)
+        if st != MUSE_OK:
+            raise MuseError(st, "muse_lmhead_forward_host")
+        return logits_host, argmax_host
+
+    def path_name(self, batch: int) -> str | None:
+        return muse_lmhead_path_name(self.handle, batch)
+
+    def launches_per_forward(self, batch: int, with_norm: bool) -> int:
+        return muse_lmhead_launches_per_forward(self.handle, batch, with_norm)
+
+    def device_status(self) -> int:
+        return muse_lmhead_device_status(self.handle)

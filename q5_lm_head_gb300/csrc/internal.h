@@ -1,0 +1,44 @@
+// Internal interface between the C-ABI layer (muse_lmhead.cu) and the kernel
+// translation units.  Not installed, not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace muse {
+
+// Device status word bits (the handle's workspace; read back by
+// muse_lmhead_device_status).
+constexpr uint32_t kStatusWaitTimeout = 1u << 0;   // a bounded mbarrier wait gave up
+
+struct Workspace {
+  unsigned long long *keys;  // [max_batch] packed argmax keys, zero between forwards
+  unsigned int *ticket;      // CTA completion counter for the argmax, zero between forwards
+  uint32_t *status;          // sticky device status bits
+  float *x;                  // [max_batch][k] normalised input (generic path)
+};
+
+struct LaunchArgs {
+  const float *hidden;   // [batch][k]
+  const float *gamma;    // [k] or nullptr
+  float eps;
+  const uint8_t *w;      // [n_rows][k/256][176]
+  float scale, cap;
+  float *logits;         // [batch][n_rows]
+  int32_t *argmax;       // [batch] or nullptr
+  int batch;
+  int64_t n_rows;
+  int k;
+  int num_sms;
+  Workspace ws;
+  cudaStream_t stream;
+};
+
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_generic(const LaunchArgs &a);     // RMSNorm pre-pass (if gamma) + generic GEMV
+bool b1_supported(int k);                            // fast batch-1 kernel compiled for this K
+cudaError_t launch_b1(const LaunchArgs &a);          // fused batch-1 kernel
+
+int generic_launches(const LaunchArgs &a);
+
+}  // namespace muse

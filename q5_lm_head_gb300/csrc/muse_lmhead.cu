@@ -1,0 +1,264 @@
+// C-ABI of the output-stage library: argument validation (fail closed, launch
+// nothing on error), handle and workspace management, kernel-path dispatch and
+// the host-buffer convenience forward.  The public contract is in
+// include/muse_lmhead.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+#include "muse_lmhead.h"
+
+struct muse_lmhead {
+  int device;
+  int64_t n_rows;
+  int64_t k;
+  int max_batch;
+  int num_sms;
+  muse::Workspace ws;
+  void *ws_base;           // single device allocation backing ws
+  float *stage_hidden;     // forward_host staging (lazy)
+  float *stage_logits;
+  int32_t *stage_argmax;
+};
+
+namespace {
+
+thread_local char g_cuda_msg[256] = "CUDA error";
+
+int cuda_fail(cudaError_t e) {
+  std::snprintf(g_cuda_msg, sizeof(g_cuda_msg), "CUDA runtime call failed: %s (%s)", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return MUSE_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    ok = (prev == dev) || cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+enum class Path { B1, Generic };
+
+Path choose_path(const muse_lmhead *h, int batch) {
+  if (batch == 1 && muse::b1_supported(static_cast<int>(h->k))) return Path::B1;
+  return Path::Generic;
+}
+
+int validate_forward(const muse_lmhead *h, const void *hidden, int batch, const float *gamma, float eps,
+                     const void *weights, float scale, float cap, const void *logits,
+                     const int32_t *argmax) {
+  if (!h || !hidden || !weights || !logits) return MUSE_ERR_NULL;
+  if (batch < 1 || batch > h->max_batch) return MUSE_ERR_BATCH;
+  if (!std::isfinite(scale) || !std::isfinite(cap)) return MUSE_ERR_VALUE;
+  if (gamma && (!std::isfinite(eps) || eps < 0.0f)) return MUSE_ERR_VALUE;
+  if (!aligned(weights, 16) || (gamma && !aligned(gamma, 16))) return MUSE_ERR_ALIGN;
+  if (argmax && !aligned(argmax, 4)) return MUSE_ERR_ALIGN;
+  return MUSE_OK;
+}
+
+int run_forward(muse_lmhead *h, const float *hidden, int batch, const float *gamma, float eps,
+                const void *weights, float scale, float cap, float *logits, int32_t *argmax,
+                cudaStream_t stream) {
+  muse::LaunchArgs a;
+  a.hidden = hidden;
+  a.gamma = gamma;
+  a.eps = eps;
+  a.w = static_cast<const uint8_t *>(weights);
+  a.scale = scale;
+  a.cap = cap;
+  a.logits = logits;
+  a.argmax = argmax;
+  a.batch = batch;
+  a.n_rows = h->n_rows;
+  a.k = static_cast<int>(h->k);
+  a.num_sms = h->num_sms;
+  a.ws = h->ws;
+  a.stream = stream;
+  cudaError_t e;
+  switch (choose_path(h, batch)) {
+    case Path::B1: e = muse::launch_b1(a); break;
+    default: e = muse::launch_generic(a); break;
+  }
+  return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k, int max_batch) {
+  if (!out) return MUSE_ERR_NULL;
+  *out = nullptr;
+  if (n_rows < 1 || n_rows > (int64_t{1} << 31) - 1 || k < 256 || k % 256 != 0 || k > (1 << 20))
+    return MUSE_ERR_SHAPE;
+  if (max_batch < 1 || max_batch > MUSE_MAX_BATCH) return MUSE_ERR_BATCH;
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (device < 0 || device >= ndev) return MUSE_ERR_DEVICE;
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (prop.major != 10 || prop.minor != 3) return MUSE_ERR_DEVICE;  // built for sm_103a only
+  DeviceGuard g(device);
+  if (!g.ok) return MUSE_ERR_DEVICE;
+
+  muse_lmhead *h = new (std::nothrow) muse_lmhead();
+  if (!h) return MUSE_ERR_NOMEM;
+  h->device = device;
+  h->n_rows = n_rows;
+  h->k = k;
+  h->max_batch = max_batch;
+  h->num_sms = prop.multiProcessorCount;
+
+  // One zeroed allocation: keys | ticket | status | x
+  const size_t keys_b = sizeof(unsigned long long) * MUSE_MAX_BATCH;
+  const size_t misc_b = 256;
+  const size_t x_b = sizeof(float) * static_cast<size_t>(max_batch) * static_cast<size_t>(k);
+  const size_t total = keys_b + misc_b + x_b;
+  void *base = nullptr;
+  e = cudaMalloc(&base, total);
+  if (e != cudaSuccess) {
+    delete h;
+    return e == cudaErrorMemoryAllocation ? MUSE_ERR_NOMEM : cuda_fail(e);
+  }
+  e = cudaMemset(base, 0, total);
+  if (e != cudaSuccess) {
+    cudaFree(base);
+    delete h;
+    return cuda_fail(e);
+  }
+  auto *p = static_cast<uint8_t *>(base);
+  h->ws_base = base;
+  h->ws.keys = reinterpret_cast<unsigned long long *>(p);
+  h->ws.ticket = reinterpret_cast<unsigned int *>(p + keys_b);
+  h->ws.status = reinterpret_cast<uint32_t *>(p + keys_b + 16);
+  h->ws.x = reinterpret_cast<float *>(p + keys_b + misc_b);
+  *out = h;
+  return MUSE_OK;
+}
+
+int muse_lmhead_forward(muse_lmhead *h, const float *hidden, int batch, const float *gamma, float eps,
+                        const void *weights, float scale, float cap, float *logits, int32_t *argmax,
+                        void *stream) {
+  int st = validate_forward(h, hidden, batch, gamma, eps, weights, scale, cap, logits, argmax);
+  if (st != MUSE_OK) return st;
+  if (!aligned(hidden, 16) || !aligned(logits, 16)) return MUSE_ERR_ALIGN;
+  DeviceGuard g(h->device);
+  if (!g.ok) return MUSE_ERR_DEVICE;
+  return run_forward(h, hidden, batch, gamma, eps, weights, scale, cap, logits, argmax,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int muse_lmhead_forward_host(muse_lmhead *h, const float *hidden_host, int batch, const float *gamma,
+                             float eps, const void *weights, float scale, float cap, float *logits_host,
+                             int32_t *argmax_host, void *stream) {
+  if (!h) return MUSE_ERR_NULL;
+  if (!logits_host && !argmax_host) return MUSE_ERR_NULL;
+  // logits_host stands in for the logits pointer in the shared checks
+  const void *out_probe = logits_host ? static_cast<const void *>(logits_host) : argmax_host;
+  int st = validate_forward(h, hidden_host, batch, gamma, eps, weights, scale, cap, out_probe, nullptr);
+  if (st != MUSE_OK) return st;
+  DeviceGuard g(h->device);
+  if (!g.ok) return MUSE_ERR_DEVICE;
+  cudaError_t e;
+  if (!h->stage_hidden) {
+    const size_t hb = sizeof(float) * h->max_batch * h->k;
+    const size_t lb = sizeof(float) * h->max_batch * h->n_rows;
+    const size_t ab = sizeof(int32_t) * MUSE_MAX_BATCH;
+    void *p1 = nullptr, *p2 = nullptr, *p3 = nullptr;
+    if ((e = cudaMalloc(&p1, hb)) != cudaSuccess || (e = cudaMalloc(&p2, lb)) != cudaSuccess ||
+        (e = cudaMalloc(&p3, ab)) != cudaSuccess) {
+      if (p1) cudaFree(p1);
+      if (p2) cudaFree(p2);
+      return e == cudaErrorMemoryAllocation ? MUSE_ERR_NOMEM : cuda_fail(e);
+    }
+    h->stage_hidden = static_cast<float *>(p1);
+    h->stage_logits = static_cast<float *>(p2);
+    h->stage_argmax = static_cast<int32_t *>(p3);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t in_b = sizeof(float) * static_cast<size_t>(batch) * h->k;
+  if ((e = cudaMemcpyAsync(h->stage_hidden, hidden_host, in_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e);
+  st = run_forward(h, h->stage_hidden, batch, gamma, eps, weights, scale, cap, h->stage_logits,
+                   argmax_host ? h->stage_argmax : nullptr, s);
+  if (st != MUSE_OK) return st;
+  if (logits_host) {
+    const size_t out_b = sizeof(float) * static_cast<size_t>(batch) * h->n_rows;
+    if ((e = cudaMemcpyAsync(logits_host, h->stage_logits, out_b, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  if (argmax_host) {
+    if ((e = cudaMemcpyAsync(argmax_host, h->stage_argmax, sizeof(int32_t) * batch, cudaMemcpyDeviceToHost,
+                             s)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+  return MUSE_OK;
+}
+
+int muse_lmhead_launches_per_forward(const muse_lmhead *h, int batch, int with_norm) {
+  if (!h) return MUSE_ERR_NULL;
+  if (batch < 1 || batch > h->max_batch) return MUSE_ERR_BATCH;
+  if (choose_path(h, batch) == Path::B1) return 1;
+  return with_norm ? 2 : 1;  // generic: RMSNorm pre-pass + GEMV
+}
+
+const char *muse_lmhead_path_name(const muse_lmhead *h, int batch) {
+  if (!h || batch < 1 || batch > h->max_batch) return nullptr;
+  switch (choose_path(h, batch)) {
+    case Path::B1: return "gemv_b1";
+    default: return "gemv_generic";
+  }
+}
+
+int muse_lmhead_device_status(muse_lmhead *h, uint32_t *status_out) {
+  if (!h || !status_out) return MUSE_ERR_NULL;
+  DeviceGuard g(h->device);
+  if (!g.ok) return MUSE_ERR_DEVICE;
+  cudaError_t e = cudaMemcpy(status_out, h->ws.status, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
+}
+
+void muse_lmhead_destroy(muse_lmhead *h) {
+  if (!h) return;
+  DeviceGuard g(h->device);
+  if (h->ws_base) cudaFree(h->ws_base);
+  if (h->stage_hidden) cudaFree(h->stage_hidden);
+  if (h->stage_logits) cudaFree(h->stage_logits);
+  if (h->stage_argmax) cudaFree(h->stage_argmax);
+  delete h;
+}
+
+const char *muse_lmhead_status_string(int status) {
+  switch (status) {
+    case MUSE_OK: return "ok";
+    case MUSE_ERR_NULL: return "a required pointer is NULL";
+    case MUSE_ERR_SHAPE: return "bad shape: need n_rows >= 1 and k a positive multiple of 256";
+    case MUSE_ERR_BATCH: return "batch outside 1..max_batch (max_batch at most 32)";
+    case MUSE_ERR_ALIGN: return "misaligned pointer: 16 bytes for hidden/gamma/weights/logits, 4 for argmax";
+    case MUSE_ERR_VALUE: return "non-finite scale or cap, or bad eps";
+    case MUSE_ERR_DEVICE: return "bad device index or not an sm_103 GPU";
+    case MUSE_ERR_CUDA: return g_cuda_msg;
+    case MUSE_ERR_NOMEM: return "out of memory";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"
