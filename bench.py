@@ -110,22 +110,25 @@ def _dist():
 
 
 def _oracle_rate(wl, hidden, gamma, wq, target_s: float):
-    """Time the oracle on a bounded row sample; returns (bytes_per_s, rows, cores, secs)."""
+    """Time the oracle, as it stands, on a bounded sample of the workload: the
+    first `rows` weight rows (all of them when they fit the time budget), run
+    `reps` times.  Returns (bytes_per_s, rows, reps, cores, secs)."""
     import numpy as np
     import oracle
     cores = oracle.default_threads()
-    rows_per_block = 2048
+    probe = min(2048, wl.n_rows)
     t0 = time.perf_counter()
-    oracle.lmhead(hidden, gamma, wq[:rows_per_block], wl.scale, wl.cap, nthreads=cores)
-    dt = time.perf_counter() - t0
-    rows = int(min(wl.n_rows, max(rows_per_block, rows_per_block * target_s / max(dt, 1e-6))))
+    oracle.lmhead(hidden, gamma, wq[:probe], wl.scale, wl.cap, nthreads=cores)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    rows = int(min(wl.n_rows, max(probe, probe * target_s / dt)))
+    reps = max(1, int(target_s / (dt * rows / probe)))
     sample = np.ascontiguousarray(wq[:rows])
     t0 = time.perf_counter()
-    oracle.lmhead(hidden, gamma, sample, wl.scale, wl.cap, nthreads=cores)
+    for _ in range(reps):
+        oracle.lmhead(hidden, gamma, sample, wl.scale, wl.cap, nthreads=cores)
     secs = time.perf_counter() - t0
-    frac = rows / wl.n_rows
-    bytes_sample = wl.algorithmic_bytes() * frac
-    return bytes_sample / secs, rows, cores, secs
+    bytes_sample = wl.algorithmic_bytes() * (rows / wl.n_rows) * reps
+    return bytes_sample / secs, rows, reps, cores, secs
 
 
 def run_reference(args, wl):
@@ -138,14 +141,15 @@ def run_reference(args, wl):
     per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         _oracle_rate(wl, hidden, gamma, wq, per_step * 0.2)
-    rates, rows_l, secs_l, cores = [], [], [], 1
+    rates, rows_l, secs_l, cores, reps = [], [], [], 1, 1
     for _ in range(args.steps):
-        r, rows, cores, secs = _oracle_rate(wl, hidden, gamma, wq, per_step)
+        r, rows, reps, cores, secs = _oracle_rate(wl, hidden, gamma, wq, per_step)
         rates.append(r)
         rows_l.append(rows)
         secs_l.append(secs)
     value = statistics.median(rates) / 1e9
-    sample = f"{int(statistics.median(rows_l))} of {wl.n_rows} rows x batch {wl.batch} per step"
+    sample = (f"{int(statistics.median(rows_l))} of {wl.n_rows} weight rows x batch {wl.batch}, "
+              f"{reps} pass(es) per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -166,6 +170,32 @@ def _config(wl, ws, l2_mode):
     return {"workload": wl.name, "n_rows": wl.n_rows, "k": wl.k, "batch": wl.batch,
             "weights": "Q5_K 176 B / 256 weights", "final_norm": wl.norm, "scale": wl.scale, "cap": wl.cap,
             "argmax": wl.argmax, "l2": l2_mode, "parallelism": f"replicas x{ws}"}
+
+
+def _e2e(args, wl, head, hidden, w_d, g_d, eps, stream, ws, nbytes):
+    """Same metric through muse_lmhead_forward_host: each step copies the pinned
+    hidden rows in and the logits + argmax out, and waits for them."""
+    import torch
+    h_pin = torch.from_numpy(hidden).pin_memory()
+    l_pin = torch.empty((wl.batch, wl.n_rows), dtype=torch.float32, pin_memory=True)
+    a_pin = torch.empty((wl.batch,), dtype=torch.int32, pin_memory=True)
+    steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        head.forward_host(h_pin, w_d, g_d, eps, wl.scale, wl.cap, l_pin, a_pin, stream)
+    if ws > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        head.forward_host(h_pin, w_d, g_d, eps, wl.scale, wl.cap, l_pin, a_pin, stream)
+    secs = (time.perf_counter() - t0) / steps
+    if ws > 1:
+        t = torch.tensor([secs], device=w_d.device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        secs = float(t.item())
+    h2d = wl.batch * wl.k * 4
+    d2h = wl.batch * wl.n_rows * 4 + wl.batch * 4
+    return {"value": round(ws * nbytes / secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "us_per_forward": round(secs * 1e6, 2)}
 
 
 def run_ours(args, wl):
@@ -245,18 +275,9 @@ def run_ours(args, wl):
     status = head.device_status()
 
     # end to end through the host-buffer entry point: pinned hidden in, logits + argmax out
-    h_pin = torch.from_numpy(hidden).pin_memory()
-    l_pin = torch.empty((wl.batch, wl.n_rows), dtype=torch.float32, pin_memory=True)
-    a_pin = torch.empty((wl.batch,), dtype=torch.int32, pin_memory=True)
-    e2e_steps = max(3, min(args.steps, 50))
-    for _ in range(2):
-        head.forward_host(h_pin, w_d, g_d, eps, wl.scale, wl.cap, l_pin, a_pin if wl.argmax else None, stream)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        head.forward_host(h_pin, w_d, g_d, eps, wl.scale, wl.cap, l_pin, a_pin if wl.argmax else None, stream)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    h2d = wl.batch * wl.k * 4
-    d2h = wl.batch * wl.n_rows * 4 + (wl.batch * 4 if wl.argmax else 0)
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(args, wl, head, hidden, w_d, g_d, eps, stream, ws, nbytes)
 
     peak, peak_kind = _measured_peaks()
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
@@ -275,17 +296,16 @@ def run_ours(args, wl):
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "kernel": head.path_name(wl.batch),
                      "algorithmic_bytes_per_launch": nbytes if head.launches_per_forward(wl.batch, wl.norm) == 1 else None},
-        "e2e": {"value": round(ws * nbytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "us_per_forward": round(e2e_s * 1e6, 2)},
+        "e2e": e2e,
         "gpu_launches": head.launches_per_forward(wl.batch, wl.norm) * args.steps,
         "clocks": clocks,
         "device_status": status,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, rows, cores, secs = _oracle_rate(wl, hidden, gamma, wq, args.cpu_seconds)
+        rate, rows, reps, cores, secs = _oracle_rate(wl, hidden, gamma, wq, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(rate / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                "sample": f"{rows} of {wl.n_rows} weight rows x batch {wl.batch} "
-                                          f"({secs:.1f} s wall on {cores} threads)"}
+                                "sample": f"{rows} of {wl.n_rows} weight rows x batch {wl.batch}, {reps} pass(es), "
+                                          f"{secs:.1f} s wall on {cores} threads"}
     head.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -303,10 +323,17 @@ def main():
     ap.add_argument("--workload", default="lmhead_b1", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="profiling: keep only the first ROWS weight rows of the workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     wl = synth.WORKLOADS[args.workload]
+    if args.rows:
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}[rows={args.rows}]", n_rows=args.rows,
+                                 boost_rows=tuple(r for r in wl.boost_rows if r < args.rows))
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -157,7 +157,9 @@ def argmax_first(out: np.ndarray) -> np.ndarray:
 
 
 def top2_gap(out: np.ndarray) -> np.ndarray:
-    """Per row: largest value minus second largest (0 when they tie)."""
+    """Per row: largest value minus second largest (0 when they tie, inf with one column)."""
     o = np.atleast_2d(out)
+    if o.shape[1] < 2:
+        return np.full(o.shape[0], np.inf)
     part = np.partition(o, -2, axis=1)
     return part[:, -1] - part[:, -2]

@@ -3,27 +3,34 @@
 // one persistent launch ("Chapter 20 — Final norm, LM head, and the soft cap",
 // §20.1 what it computes, §20.3 the 924.6 MB weight stream, §20.4 the cap).
 //
-// Layout of the work
-//   * A tile is kRows consecutive weight rows: kRows * (K/256) * 176 bytes,
-//     contiguous in HBM.  CTAs take tiles round-robin (tile = blockIdx.x +
-//     i * gridDim.x), so at any moment the whole GPU streams one contiguous
-//     stretch of the matrix.
-//   * One producer warp moves tiles into a ring of shared-memory stages with
-//     1-D bulk copies (cp.async.bulk, mbarrier transaction counts, L2
-//     evict-first); consumers release stages through "empty" mbarriers.  Every
-//     wait is bounded.
-//   * Consumer thread (kb, c) owns 64 columns: block kb, sub-blocks 2c and 2c+1.
-//     Its 64 normalised activations live in registers for the whole launch
-//     (column-stationary), so shared memory carries weights only.  The CTA has
-//     four such teams ("streams"), each taking every fourth row of a tile.
-//   * Per sub-block s the thread forms sum_j q_j x_j.  A 5-bit q is turned into
-//     the float 1 + q/128 by placing (0x80 | q) under the exponent byte 0x3F
-//     with one byte permute; the chain starts at -sum_j x_j, so it ends at
-//     sum_j q_j x_j / 128 with no integer->float conversion per weight.  Then
-//     raw += d*128*sc_s*that - dmin*m_s*sum_j x_j.
-//   * Per-row partials (one per thread) meet in shared memory; one warp per row
-//     sums them, applies scale and cap, stores the logit and keeps the running
-//     argmax key.
+// Warp roles (one CTA per SM)
+//   * consumer warps: thread (kb, c) owns 64 columns, block kb, sub-blocks 2c
+//     and 2c+1, for the whole launch (column-stationary).  Four teams of such
+//     threads ("streams") split the rows of a tile.  The four threads of one
+//     block add their row contributions with two shuffles and one of them
+//     writes the block's partial into a ring of partial slots.  Consumers wait
+//     for nothing but "stage full".
+//   * producer warp: moves tiles of kRows consecutive weight rows (contiguous
+//     in HBM) into a ring of shared-memory stages with 1-D bulk copies
+//     (cp.async.bulk + mbarrier transaction counts, L2 evict-first).  CTAs take
+//     tiles round-robin, so the whole GPU streams one contiguous stretch.  Each
+//     time consumers release a stage, the warp first re-arms it with the next
+//     tile and then finishes the released stage's rows: fixed-order sum of the
+//     block partials, scale + soft cap, store, argmax key.  The partial ring
+//     has one slot more than the stage ring, so a slot is never rewritten
+//     before the producer has read it (the rewrite needs a stage the producer
+//     arms only afterwards).
+//
+// Arithmetic of a consumer thread (exact up to f32 rounding of the last steps)
+//   Its 64 normalised activations x_j are written as x_j = sigma * xi_j with a
+//   per-thread sigma = max|x| / 8388600 and 24-bit integers xi_j, stored as three
+//   byte planes xi = 65536*x2 + 256*x1 + x0 (x2 signed, x1 and x0 unsigned).
+//   For each sub-block s, sum_j q_j xi_j is built with dp4a on four 5-bit quants
+//   per word (low nibble | high bit << 4; high nibbles are taken as 2q so no
+//   extra shift is needed) against each plane, in exact integer arithmetic.
+//   Then raw += d * sigma * sum_s sc_s * (that) - dmin * sum_s m_s * sum_j x_j,
+//   which is sum_j (d*sc_s*q_j - dmin*m_s) x_j up to rounding (§20.1 matvec
+//   with the Q5_K weight w = d*sc*q - dmin*m).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -34,32 +41,115 @@ namespace muse {
 namespace {
 
 constexpr int kRows = 8;            // weight rows per pipeline stage
-constexpr int kStreams = 4;         // row teams per CTA
-constexpr int kMaxSmem = 227 * 1024;
+constexpr int kStreams = 4;         // row teams of consumer threads
+constexpr int kMaxSmem = 227 * 1024 - 1024;   // opt-in limit minus static shared memory
+constexpr float kQuantMax = 8388600.0f;   // |xi| stays below 2^23 after rounding
 
 template <int NB>
 struct B1Cfg {
   static constexpr int kUnits = 4 * NB;                    // (block, 64-column group) units per row
   static constexpr int kConsumers = kUnits * kStreams;
   static_assert(kConsumers % 32 == 0, "consumer threads must fill whole warps");
+  static_assert(kUnits % 4 == 0, "the four units of a block stay inside one stream");
   static constexpr int kConsumerWarps = kConsumers / 32;
-  static_assert(kConsumerWarps >= kRows, "one reducing warp per row of a stage");
-  static constexpr int kThreads = kConsumers + 32;         // + one producer warp
+  static constexpr int kProducerWarp = kConsumerWarps;
+  static constexpr int kThreads = kConsumers + 32;
   static constexpr int kRowBytes = NB * kBlockBytes;
   static constexpr int kStageBytes = kRows * kRowBytes;
-  static constexpr int kPartialBytes = 2 * kRows * kUnits * 4;
-  static constexpr int kFixedBytes = kPartialBytes + 1024;  // partials + barriers + scratch
-  static constexpr int kStagesFit = (kMaxSmem - kFixedBytes) / kStageBytes;
+  static constexpr int kSlotBytes = kRows * NB * 4;         // one partial per (row, block)
+  static constexpr int kFixedBytes = 512;                   // barriers + scratch
+  static constexpr int kStagesFit = (kMaxSmem - kFixedBytes - kSlotBytes) / (kStageBytes + kSlotBytes);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static_assert(kStages >= 2, "need at least double buffering");
-  static constexpr int kSmemBytes = kStages * kStageBytes + kFixedBytes;
+  static constexpr int kSlots = kStages + 1;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kSlots * kSlotBytes + kFixedBytes;
+  static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
 };
 
-// 1 + q/128 as a float, from byte `t` of Q (that byte holds 0x80 | q, q < 32).
-template <int T>
-__device__ __forceinline__ float q_as_float(uint32_t q4) {
-  // result bytes (high..low): 0x3F, Q.byte[T], 0x00, 0x00
-  return __uint_as_float(__byte_perm(q4, 0x3Fu, 0x4055u | (T << 8)));
+__device__ __forceinline__ uint32_t rotl32(uint32_t v, uint32_t s) { return __funnelshift_l(v, v, s); }
+
+// Four bytes, one per 4 consecutive activations, of the 24-bit integer planes.
+struct XPlanes {
+  uint32_t p2[8], p1[8], p0[8];   // word i holds positions 4i..4i+3
+};
+
+__device__ __forceinline__ void quantize_planes(const float (&x)[32], float inv, XPlanes &out) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t w2 = 0, w1 = 0, w0 = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int xi = __float2int_rn(x[4 * i + t] * inv);
+      w2 |= (static_cast<uint32_t>(xi >> 16) & 0xFFu) << (8 * t);
+      w1 |= (static_cast<uint32_t>(xi >> 8) & 0xFFu) << (8 * t);
+      w0 |= (static_cast<uint32_t>(xi) & 0xFFu) << (8 * t);
+    }
+    out.p2[i] = w2;
+    out.p1[i] = w1;
+    out.p0[i] = w0;
+  }
+}
+
+// Per-thread constants that select this thread's sub-blocks 2c and 2c+1.
+struct UnitSel {
+  uint32_t rot;        // rotate that brings bit 2c of each qh byte to bit 4
+  uint32_t sh_sc, sh_m, msk_lo, sh_hi2, msk_hi;
+  bool upper;          // sub-blocks 4..7: scales split over two bytes
+  int qs_off;          // byte offset of this thread's 32 low-nibble bytes
+};
+
+__device__ __forceinline__ UnitSel make_unit_sel(int c) {
+  UnitSel u;
+  u.upper = c >= 2;
+  u.sh_sc = u.upper ? 16u * (c - 2) : 16u * c;
+  u.sh_m = u.upper ? 16u * (c - 2) + 4u : 16u * c;
+  u.msk_lo = u.upper ? 0x0F0Fu : 0x3F3Fu;
+  u.sh_hi2 = u.upper ? 16u * (c - 2) + 2u : 0u;
+  u.msk_hi = u.upper ? 0x3030u : 0u;
+  u.rot = static_cast<uint32_t>(4 - 2 * c) & 31u;
+  u.qs_off = kOffQs + 32 * c;
+  return u;
+}
+
+// This thread's contribution to one row: sum over its 64 columns of
+// (d*sc_s*q - dmin*m_s) * x, from the row's Q5_K block `blk` in shared memory.
+__device__ __forceinline__ float unit_partial(const uint8_t *blk, const UnitSel &us, const XPlanes &xl,
+                                              const XPlanes &xh, float sx_lo, float sx_hi, float sigma_half) {
+  const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+  const uint4 qh0 = *reinterpret_cast<const uint4 *>(blk + kOffQh);
+  const uint4 qh1 = *reinterpret_cast<const uint4 *>(blk + kOffQh + 16);
+  const uint4 qs0 = *reinterpret_cast<const uint4 *>(blk + us.qs_off);
+  const uint4 qs1 = *reinterpret_cast<const uint4 *>(blk + us.qs_off + 16);
+  const uint32_t H[8] = {qh0.x, qh0.y, qh0.z, qh0.w, qh1.x, qh1.y, qh1.z, qh1.w};
+  const uint32_t A[8] = {qs0.x, qs0.y, qs0.z, qs0.w, qs1.x, qs1.y, qs1.z, qs1.w};
+  int l2 = 0, h2 = 0;
+  unsigned l1 = 0, l0 = 0, h1 = 0, h0 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t t = rotl32(H[i], us.rot);                             // high bits at 4 (lo) and 5 (hi)
+    const uint32_t qlo = (A[i] & 0x0F0F0F0Fu) | (t & 0x10101010u);       // q
+    const uint32_t qhi = ((A[i] >> 3) & 0x1E1E1E1Eu) | (t & 0x20202020u);  // 2q
+    l2 = __dp4a(static_cast<int>(qlo), static_cast<int>(xl.p2[i]), l2);
+    l1 = __dp4a(qlo, xl.p1[i], l1);
+    l0 = __dp4a(qlo, xl.p0[i], l0);
+    h2 = __dp4a(static_cast<int>(qhi), static_cast<int>(xh.p2[i]), h2);
+    h1 = __dp4a(qhi, xh.p1[i], h1);
+    h0 = __dp4a(qhi, xh.p0[i], h0);
+  }
+  // scales and mins of sub-blocks 2c (low byte) and 2c+1 (high byte)
+  const uint32_t wsc = us.upper ? hdr.w : hdr.y;
+  const uint32_t wm = us.upper ? hdr.w : hdr.z;
+  const uint32_t scp = ((wsc >> us.sh_sc) & us.msk_lo) | ((hdr.y >> us.sh_hi2) & us.msk_hi);
+  const uint32_t mp = ((wm >> us.sh_m) & us.msk_lo) | ((hdr.z >> us.sh_hi2) & us.msk_hi);
+  const int sc_lo2 = static_cast<int>((scp & 0xFFu) << 1);   // x2: low nibbles carry q, high 2q
+  const int sc_hi = static_cast<int>(scp >> 8);
+  const int a2 = l2 * sc_lo2 + h2 * sc_hi;
+  const int a1 = static_cast<int>(l1) * sc_lo2 + static_cast<int>(h1) * sc_hi;
+  const int a0 = static_cast<int>(l0) * sc_lo2 + static_cast<int>(h0) * sc_hi;
+  const float dotv = fmaf(static_cast<float>(a2), 65536.0f, fmaf(static_cast<float>(a1), 256.0f, static_cast<float>(a0)));
+  const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));   // (d, dmin)
+  const float mins = fmaf(static_cast<float>(mp & 0xFFu), sx_lo, static_cast<float>(mp >> 8) * sx_hi);
+  return fmaf(dd.x * sigma_half, dotv, -dd.y * mins);
 }
 
 template <int NB>
@@ -72,12 +162,12 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
   constexpr int K = NB * kBlockWeights;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *stages = smem;
-  float *partial = reinterpret_cast<float *>(smem + C::kStages * C::kStageBytes);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes + C::kPartialBytes);
+  float *slots = reinterpret_cast<float *>(smem + C::kStages * C::kStageBytes);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes + C::kSlots * C::kSlotBytes);
   uint64_t *empty = full + C::kStages;
-  float *s_red = reinterpret_cast<float *>(empty + C::kStages);           // [32]
+  float *s_red = reinterpret_cast<float *>(empty + C::kStages);            // [32]
   unsigned long long *s_best = reinterpret_cast<unsigned long long *>(s_red + 32);
-  uint32_t *s_abort = reinterpret_cast<uint32_t *>(s_best + 1);
+  volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(s_best + 1);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -94,35 +184,75 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
   }
   __syncthreads();
 
-  if (warp == C::kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t policy = ptx::policy_evict_first();
-      int64_t issued = 0;
-      for (int64_t it = 0;; ++it) {
-        const int64_t tile = blockIdx.x + it * gridDim.x;
-        if (tile >= n_tiles) break;
-        const int st = static_cast<int>(it % C::kStages);
-        if (it >= C::kStages) {
-          const uint32_t par = static_cast<uint32_t>((it / C::kStages - 1) & 1);
-          if (*reinterpret_cast<volatile uint32_t *>(s_abort) || !ptx::mbar_wait(&empty[st], par)) {
-            atomicOr(status, kStatusWaitTimeout);
-            *reinterpret_cast<volatile uint32_t *>(s_abort) = 1u;
-            break;
-          }
-        }
+  auto fail = [&]() {
+    atomicOr(status, kStatusWaitTimeout);
+    *s_abort = 1u;
+  };
+
+  if (warp == C::kProducerWarp) {
+    // ------------------------------------------------------------ producer + row epilogue
+    const uint64_t policy = ptx::policy_evict_first();
+    const int er = lane >> 2, eq = lane & 3;   // epilogue: row er, every 4th block partial from eq
+    unsigned long long best = 0ull;
+    // finish the rows of stage j (its consumers have released it)
+    auto finish = [&](int j) {
+      const int64_t r0 = (blockIdx.x + static_cast<int64_t>(j) * gridDim.x) * kRows;
+      const float *pr = slots + (j % C::kSlots) * (C::kSlotBytes / 4) + er * NB;
+      float sacc = 0.0f;
+#pragma unroll
+      for (int g = 0; g < NB; g += 4)
+        if (g + eq < NB) sacc += pr[g + eq];
+      sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
+      sacc += __shfl_xor_sync(0xffffffffu, sacc, 2);
+      if (eq == 0 && r0 + er < n_rows) {
+        const int64_t row = r0 + er;
+        const float out = scale_softcap(sacc, scale, cap);
+        logits[row] = out;
+        best = umax64(best, argmax_key(out, static_cast<uint32_t>(row)));
+      }
+      __syncwarp();
+    };
+    auto wait_released = [&](int j) -> bool {   // all lanes; lane 0 polls
+      bool ok = true;
+      if (lane == 0) ok = ptx::mbar_wait(&empty[j % C::kStages], static_cast<uint32_t>((j / C::kStages) & 1));
+      return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    };
+    int issued = 0, st = 0;
+    bool aborted = false;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      if (__any_sync(0xffffffffu, *s_abort != 0u)) { aborted = true; break; }
+      if (issued >= C::kStages && !wait_released(issued - C::kStages)) {
+        if (lane == 0) fail();
+        aborted = true;
+        break;
+      }
+      if (lane == 0) {
         const int64_t r0 = tile * kRows;
-        const int rows = static_cast<int>(n_rows - r0 < kRows ? n_rows - r0 : kRows);
+        const int rows = n_rows - r0 < kRows ? static_cast<int>(n_rows - r0) : kRows;
         const uint32_t bytes = static_cast<uint32_t>(rows * C::kRowBytes);
         ptx::mbar_arrive_expect_tx(&full[st], bytes);
         ptx::bulk_g2s(stages + st * C::kStageBytes, w + r0 * C::kRowBytes, bytes, &full[st], policy);
-        issued = it + 1;
       }
-      // Never leave the CTA with copies in flight: wait (bounded) for the last
-      // stage fills this warp armed.  In a normal run they completed long ago.
-      for (int64_t it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
-        ptx::mbar_wait(&full[it % C::kStages], static_cast<uint32_t>((it / C::kStages) & 1));
+      if (issued >= C::kStages) finish(issued - C::kStages);
+      ++issued;
+      if (++st == C::kStages) st = 0;
     }
+    const int first = issued > C::kStages ? issued - C::kStages : 0;
+    for (int j = first; j < issued && !aborted; ++j) {
+      if (__any_sync(0xffffffffu, *s_abort != 0u) || !wait_released(j)) {
+        if (lane == 0) fail();
+        aborted = true;
+        break;
+      }
+      finish(j);
+    }
+    if (aborted && lane == 0) {
+      // never leave the CTA with copies in flight: wait (bounded) for the fills armed last
+      for (int j = first; j < issued; ++j)
+        ptx::mbar_wait(&full[j % C::kStages], static_cast<uint32_t>((j / C::kStages) & 1));
+    }
+    for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
+    if (lane == 0) *s_best = best;
   } else {
     // ------------------------------------------------------------ consumers
     const int stream = tid / C::kUnits;
@@ -147,106 +277,82 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
       for (int i = 0; i < C::kConsumerWarps; ++i) tot += s_red[i];
       r = 1.0f / sqrtf(tot / static_cast<float>(K) + eps);
     }
-    // This thread's 64 activations: x_lo[l] for sub-block 2c, x_hi[l] for 2c+1.
-    float x_lo[32], x_hi[32];
-    const int col = kb * kBlockWeights + 64 * c;
+    // This thread's 64 activations, x_lo for sub-block 2c and x_hi for 2c+1.
+    XPlanes xl, xh;
+    float sx_lo = 0.0f, sx_hi = 0.0f, sigma_half;
+    {
+      float x_lo[32], x_hi[32];
+      const int col = kb * kBlockWeights + 64 * c;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float4 hl = *reinterpret_cast<const float4 *>(hidden + col + 4 * i);
-      float4 hh = *reinterpret_cast<const float4 *>(hidden + col + 32 + 4 * i);
-      if (gamma) {
-        const float4 gl = *reinterpret_cast<const float4 *>(gamma + col + 4 * i);
-        const float4 gh = *reinterpret_cast<const float4 *>(gamma + col + 32 + 4 * i);
-        hl = make_float4(hl.x * r * gl.x, hl.y * r * gl.y, hl.z * r * gl.z, hl.w * r * gl.w);
-        hh = make_float4(hh.x * r * gh.x, hh.y * r * gh.y, hh.z * r * gh.z, hh.w * r * gh.w);
-      }
-      x_lo[4 * i + 0] = hl.x; x_lo[4 * i + 1] = hl.y; x_lo[4 * i + 2] = hl.z; x_lo[4 * i + 3] = hl.w;
-      x_hi[4 * i + 0] = hh.x; x_hi[4 * i + 1] = hh.y; x_hi[4 * i + 2] = hh.z; x_hi[4 * i + 3] = hh.w;
-    }
-    float sx_lo = 0.0f, sx_hi = 0.0f;
-#pragma unroll
-    for (int l = 0; l < 32; ++l) {
-      sx_lo += x_lo[l];
-      sx_hi += x_hi[l];
-    }
-    const int sh_lo = 2 * c, sh_hi = 2 * c + 1;   // qh bit of each sub-block
-
-    unsigned long long best = 0ull;
-    for (int64_t it = 0;; ++it) {
-      const int64_t tile = blockIdx.x + it * gridDim.x;
-      if (tile >= n_tiles) break;
-      const int st = static_cast<int>(it % C::kStages);
-      const bool ok = ptx::mbar_wait(&full[st], static_cast<uint32_t>((it / C::kStages) & 1));
-      const int64_t r0 = tile * kRows;
-      const int rows = static_cast<int>(n_rows - r0 < kRows ? n_rows - r0 : kRows);
-      float *part = partial + (it & 1) * (kRows * C::kUnits);
-      const uint8_t *sbase = stages + st * C::kStageBytes;
-#pragma unroll 1
-      for (int rr = 0; rr < kRows / kStreams; ++rr) {
-        const int rl = stream + rr * kStreams;
-        if (ok && rl < rows) {
-          const uint8_t *blk = sbase + rl * C::kRowBytes + kb * kBlockBytes;
-          const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-          const uint4 qh0 = *reinterpret_cast<const uint4 *>(blk + kOffQh);
-          const uint4 qh1 = *reinterpret_cast<const uint4 *>(blk + kOffQh + 16);
-          const uint4 qs0 = *reinterpret_cast<const uint4 *>(blk + kOffQs + 32 * c);
-          const uint4 qs1 = *reinterpret_cast<const uint4 *>(blk + kOffQs + 32 * c + 16);
-          const uint32_t H[8] = {qh0.x, qh0.y, qh0.z, qh0.w, qh1.x, qh1.y, qh1.z, qh1.w};
-          const uint32_t A[8] = {qs0.x, qs0.y, qs0.z, qs0.w, qs1.x, qs1.y, qs1.z, qs1.w};
-          float acc_lo0 = -sx_lo, acc_lo1 = 0.0f, acc_hi0 = -sx_hi, acc_hi1 = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t qlo = (A[i] & 0x0F0F0F0Fu) | (((H[i] >> sh_lo) & 0x01010101u) << 4) | 0x80808080u;
-            const uint32_t qhi = ((A[i] >> 4) & 0x0F0F0F0Fu) | (((H[i] >> sh_hi) & 0x01010101u) << 4) | 0x80808080u;
-            acc_lo0 = fmaf(q_as_float<0>(qlo), x_lo[4 * i + 0], acc_lo0);
-            acc_lo1 = fmaf(q_as_float<1>(qlo), x_lo[4 * i + 1], acc_lo1);
-            acc_lo0 = fmaf(q_as_float<2>(qlo), x_lo[4 * i + 2], acc_lo0);
-            acc_lo1 = fmaf(q_as_float<3>(qlo), x_lo[4 * i + 3], acc_lo1);
-            acc_hi0 = fmaf(q_as_float<0>(qhi), x_hi[4 * i + 0], acc_hi0);
-            acc_hi1 = fmaf(q_as_float<1>(qhi), x_hi[4 * i + 1], acc_hi1);
-            acc_hi0 = fmaf(q_as_float<2>(qhi), x_hi[4 * i + 2], acc_hi0);
-            acc_hi1 = fmaf(q_as_float<3>(qhi), x_hi[4 * i + 3], acc_hi1);
-          }
-          const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
-          const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
-          int sc0, m0, sc1, m1;
-          q5k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c, sc0, m0);
-          q5k_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + 1, sc1, m1);
-          const float dot_lo = acc_lo0 + acc_lo1;   // sum q x / 128 over sub-block 2c
-          const float dot_hi = acc_hi0 + acc_hi1;
-          const float main = fmaf(static_cast<float>(sc0), dot_lo, static_cast<float>(sc1) * dot_hi);
-          const float mins = fmaf(static_cast<float>(m0), sx_lo, static_cast<float>(m1) * sx_hi);
-          part[rl * C::kUnits + u] = fmaf(d * 128.0f, main, -dmin * mins);
+      for (int i = 0; i < 8; ++i) {
+        float4 hl = *reinterpret_cast<const float4 *>(hidden + col + 4 * i);
+        float4 hh = *reinterpret_cast<const float4 *>(hidden + col + 32 + 4 * i);
+        if (gamma) {
+          const float4 gl = *reinterpret_cast<const float4 *>(gamma + col + 4 * i);
+          const float4 gh = *reinterpret_cast<const float4 *>(gamma + col + 32 + 4 * i);
+          hl = make_float4(hl.x * r * gl.x, hl.y * r * gl.y, hl.z * r * gl.z, hl.w * r * gl.w);
+          hh = make_float4(hh.x * r * gh.x, hh.y * r * gh.y, hh.z * r * gh.z, hh.w * r * gh.w);
         }
+        x_lo[4 * i + 0] = hl.x; x_lo[4 * i + 1] = hl.y; x_lo[4 * i + 2] = hl.z; x_lo[4 * i + 3] = hl.w;
+        x_hi[4 * i + 0] = hh.x; x_hi[4 * i + 1] = hh.y; x_hi[4 * i + 2] = hh.z; x_hi[4 * i + 3] = hh.w;
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int l = 0; l < 32; ++l) {
+        sx_lo += x_lo[l];
+        sx_hi += x_hi[l];
+        amax = fmaxf(amax, fmaxf(fabsf(x_lo[l]), fabsf(x_hi[l])));
+      }
+      const float inv = amax > 0.0f ? kQuantMax / amax : 0.0f;
+      sigma_half = amax > 0.0f ? 0.5f / inv : 0.0f;   // the 1/2 undoes the 2q form of the high nibbles
+      quantize_planes(x_lo, inv, xl);
+      quantize_planes(x_hi, inv, xh);
+    }
+    const UnitSel us = make_unit_sel(c);
+
+    int st = 0, ps = 0;
+    uint32_t ph = 0;                           // round parity of the stage ring
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      // every exit decision is taken by the whole warp (the loop body shuffles)
+      if (__any_sync(0xffffffffu, *s_abort != 0u)) break;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full[st], ph))) {
+        if (lane == 0) fail();
+        break;
+      }
+      const int64_t r0 = tile * kRows;
+      const int rows = n_rows - r0 < kRows ? static_cast<int>(n_rows - r0) : kRows;
+      float *slot = slots + ps * (C::kSlotBytes / 4) + kb;
+      const uint8_t *sbase = stages + st * C::kStageBytes + kb * kBlockBytes;
+      float pv[kRows / kStreams];
+      if (rows == kRows) {
+#pragma unroll
+        for (int rr = 0; rr < kRows / kStreams; ++rr)
+          pv[rr] = unit_partial(sbase + (stream + rr * kStreams) * C::kRowBytes, us, xl, xh, sx_lo, sx_hi,
+                                sigma_half);
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < kRows / kStreams; ++rr) {
+          const int rl = stream + rr * kStreams;
+          pv[rr] = rl < rows ? unit_partial(sbase + rl * C::kRowBytes, us, xl, xh, sx_lo, sx_hi, sigma_half)
+                             : 0.0f;
+        }
+      }
+#pragma unroll
+      for (int rr = 0; rr < kRows / kStreams; ++rr) {
+        float v = pv[rr];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);   // the four units of block kb
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (c == 0) slot[(stream + rr * kStreams) * NB] = v;
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[st]);
-      // All consumers learn together whether any of them timed out, so none is
-      // left waiting at a barrier the others have abandoned.
-      if (ptx::named_bar_red_or(1, C::kConsumers, !ok)) {
-        if (tid == 0) {
-          atomicOr(status, kStatusWaitTimeout);
-          *reinterpret_cast<volatile uint32_t *>(s_abort) = 1u;
-        }
-        break;
-      }
-      if (warp < rows) {
-        float s = 0.0f;
-        for (int j = lane; j < C::kUnits; j += 32) s += part[warp * C::kUnits + j];
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) {
-          const int64_t row = r0 + warp;
-          const float out = scale_softcap(s, scale, cap);
-          logits[row] = out;
-          best = umax64(best, argmax_key(out, static_cast<uint32_t>(row)));
-        }
-      }
+      if (++st == C::kStages) { st = 0; ph ^= 1u; }
+      if (++ps == C::kSlots) ps = 0;
     }
-    if (argmax && lane == 0 && best != 0ull) atomicMax(s_best, best);
   }
 
+  __syncthreads();
   if (argmax) {
-    __syncthreads();
     if (tid == 0 && *s_best != 0ull) atomicMax(keys, *s_best);
     argmax_finish(keys, ticket, argmax, 1);
   }

@@ -10,7 +10,8 @@
 namespace muse {
 namespace ptx {
 
-constexpr uint32_t kSpinLimit = 1u << 22;  // polls (with back-off) before a wait gives up
+constexpr uint32_t kSpinLimit = 1u << 16;      // polls before a wait gives up
+constexpr uint32_t kSuspendHintNs = 20000u;     // each poll may sleep this long (woken on completion)
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -35,24 +36,25 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One poll; the thread may be suspended for up to kSuspendHintNs while the
+// phase is incomplete and is woken when it completes.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
+// Wait for the phase with the given parity to complete; false on timeout
+// (at most kSpinLimit polls, about kSpinLimit * kSuspendHintNs).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
-    if (i >= 32) __nanosleep(64);
-  }
   return false;
 }
 
