@@ -124,6 +124,35 @@ const char *muse_lmhead_path_name(const muse_lmhead *h, int batch);
  */
 int muse_lmhead_device_status(muse_lmhead *h, uint32_t *status_out);
 
+/*
+ * Batch-1 forward for callers that cannot allocate device memory at call time
+ * (code running during CUDA graph capture, runtimes that reserve all device
+ * memory through their own allocator, serving loops that must not risk the
+ * implicit synchronisation of cudaMalloc).  No handle: the few bytes of
+ * scratch the fused kernel needs (argmax key, completion ticket, status word)
+ * live in a fixed 256-byte array inside the library's device memory, which
+ * every GPU that loads the library holds until the process exits.  The pages
+ * have no counterpart of this call; it is a deployment convenience.
+ *   device   CUDA device the pointers live on (made current for the call).
+ *   hidden   [k] f32, one row; gamma/eps/weights/scale/cap/logits/argmax as for
+ *            muse_lmhead_forward with batch 1 (logits [n_rows], argmax [1]).
+ *   n_rows   1 .. 2^31-1;  k: 4,096 or 6,656 only (the fused kernel's widths),
+ *            anything else is rejected with MUSE_ERR_SHAPE before any launch.
+ * Calls no cudaMalloc/cudaFree and no allocating library routine.  It clears
+ * its scratch with an asynchronous 16-byte memset on `stream`, then launches
+ * the kernel.  The first call on a device performs one-time set-up (looks up
+ * the scratch array's device address, sets the kernel's shared-memory limit);
+ * make that first call before any stream capture.  All calls on a device share
+ * the scratch: calls that may overlap on the GPU race on it and must be
+ * ordered by the caller (same stream, or events).
+ */
+int muse_lmhead_forward_b1_noalloc(int device, const float *hidden,
+                                   const float *gamma, float eps,
+                                   const void *weights, int64_t n_rows,
+                                   int64_t k, float scale, float cap,
+                                   float *logits, int32_t *argmax,
+                                   void *stream);
+
 /* Free the handle and its workspace.  NULL is allowed.  Must not be called
  * while a forward using the handle may still be running on the GPU. */
 void muse_lmhead_destroy(muse_lmhead *h);

@@ -18,7 +18,8 @@ __all__ = [
     "LMHead", "MuseError", "library_path", "load_library",
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
-    "muse_lmhead_destroy", "muse_lmhead_status_string", "EXPORTED_SYMBOLS",
+    "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
+    "EXPORTED_SYMBOLS",
     "LOGIT_SCALE", "SOFTCAP", "RMS_EPS",
 ]
 
@@ -35,7 +36,7 @@ RMS_EPS = 1e-5
 EXPORTED_SYMBOLS = (
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
-    "muse_lmhead_destroy", "muse_lmhead_status_string",
+    "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
 )
 
 MUSE_OK = 0
@@ -82,6 +83,8 @@ def load_library():
     lib.muse_lmhead_destroy.argtypes = [vp]
     lib.muse_lmhead_status_string.restype = ctypes.c_char_p
     lib.muse_lmhead_status_string.argtypes = [i32]
+    lib.muse_lmhead_forward_b1_noalloc.restype = i32
+    lib.muse_lmhead_forward_b1_noalloc.argtypes = [i32, vp, vp, f32, vp, i64, i64, f32, f32, vp, vp, vp]
     _lib = lib
     return lib
 
@@ -129,6 +132,14 @@ def muse_lmhead_device_status(h: int) -> int:
 def muse_lmhead_destroy(h: int | None) -> None:
     if h:
         load_library().muse_lmhead_destroy(h)
+
+
+def muse_lmhead_forward_b1_noalloc(device: int, hidden: int, gamma: int | None, eps: float, weights: int,
+                                   n_rows: int, k: int, scale: float, cap: float, logits: int,
+                                   argmax: int | None, stream: int | None) -> int:
+    """Batch-1 forward without a handle that allocates no device memory (see the C header)."""
+    return load_library().muse_lmhead_forward_b1_noalloc(device, hidden, gamma, eps, weights, n_rows, k, scale,
+                                                         cap, logits, argmax, stream)
 
 
 def muse_lmhead_status_string(status: int) -> str:
