@@ -102,6 +102,35 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ncu summaries that carry a per-launch DRAM traffic figure: (file, workload, kernel sources)
+_PROFILED = {"gemv_b1": ("gemv_b1_lmhead.md", "lmhead_b1", ("gemv_b1.cu", "common.cuh", "ptx.cuh"))}
+
+
+def _profiled_traffic(kernel_path: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when there
+    is none for this kernel/workload or the kernel source changed since."""
+    import hashlib
+    ent = _PROFILED.get(kernel_path)
+    if not ent or ent[1] != workload:
+        return None
+    csrc = os.path.join(ROOT, "q5_lm_head_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ent[2]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    digest, traffic = None, None
+    try:
+        with open(os.path.join(ROOT, "profiles", ent[0])) as fh:
+            for line in fh:
+                if line.startswith("kernel-source:"):
+                    digest = line.split()[1]
+                elif line.startswith("traffic_bytes_per_launch:"):
+                    traffic = int(line.split()[1])
+    except OSError:
+        return None
+    return traffic if digest and h.hexdigest().startswith(digest) else None
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -292,7 +321,8 @@ def run_ours(args, wl):
         "pct_of_peak": round(100.0 * achieved / peak, 2),
         "kernel_path": head.path_name(wl.batch),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": _profiled_traffic(head.path_name(wl.batch), wl.name),
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "kernel": head.path_name(wl.batch),
                      "algorithmic_bytes_per_launch": nbytes if head.launches_per_forward(wl.batch, wl.norm) == 1 else None},
