@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace muse {
@@ -16,6 +17,7 @@ struct Workspace {
   unsigned int *ticket;      // CTA completion counter for the argmax, zero between forwards
   uint32_t *status;          // sticky device status bits
   float *x;                  // [max_batch][k] normalised input (generic path)
+  uint8_t *xpkg;             // per-block activation packages (tensor-core path)
 };
 
 struct LaunchArgs {
@@ -40,5 +42,11 @@ bool b1_supported(int k);                            // fast batch-1 kernel comp
 cudaError_t launch_b1(const LaunchArgs &a);          // fused batch-1 kernel
 
 int generic_launches(const LaunchArgs &a);
+
+// Tensor-core path (batches 2..32): activation-package prep + tcgen05 kernel.
+bool tc_supported(int batch);
+size_t tc_workspace_bytes(int k);
+cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_rows, int k);
+cudaError_t launch_tc(const LaunchArgs &a, const CUtensorMap &map);
 
 }  // namespace muse

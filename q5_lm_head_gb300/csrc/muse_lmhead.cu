@@ -22,6 +22,8 @@ struct muse_lmhead {
   int num_sms;
   muse::Workspace ws;
   void *ws_base;           // single device allocation backing ws
+  CUtensorMap wmap;        // weight tensor map of the tensor-core path, for wmap_ptr
+  const void *wmap_ptr;
   float *stage_hidden;     // forward_host staging (lazy)
   float *stage_logits;
   int32_t *stage_argmax;
@@ -52,10 +54,11 @@ struct DeviceGuard {
   }
 };
 
-enum class Path { B1, Generic };
+enum class Path { B1, TensorCore, Generic };
 
 Path choose_path(const muse_lmhead *h, int batch) {
   if (batch == 1 && muse::b1_supported(static_cast<int>(h->k))) return Path::B1;
+  if (muse::tc_supported(batch)) return Path::TensorCore;
   return Path::Generic;
 }
 
@@ -92,6 +95,14 @@ int run_forward(muse_lmhead *h, const float *hidden, int batch, const float *gam
   cudaError_t e;
   switch (choose_path(h, batch)) {
     case Path::B1: e = muse::launch_b1(a); break;
+    case Path::TensorCore:
+      if (h->wmap_ptr != weights) {
+        e = muse::tc_encode_weights(&h->wmap, weights, h->n_rows, static_cast<int>(h->k));
+        if (e != cudaSuccess) break;
+        h->wmap_ptr = weights;
+      }
+      e = muse::launch_tc(a, h->wmap);
+      break;
     default: e = muse::launch_generic(a); break;
   }
   return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
@@ -126,11 +137,12 @@ int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k, i
   h->max_batch = max_batch;
   h->num_sms = prop.multiProcessorCount;
 
-  // One zeroed allocation: keys | ticket | status | x
+  // One zeroed allocation: keys | ticket | status | x | activation packages
   const size_t keys_b = sizeof(unsigned long long) * MUSE_MAX_BATCH;
   const size_t misc_b = 256;
   const size_t x_b = sizeof(float) * static_cast<size_t>(max_batch) * static_cast<size_t>(k);
-  const size_t total = keys_b + misc_b + x_b;
+  const size_t pkg_b = max_batch >= 2 ? muse::tc_workspace_bytes(static_cast<int>(k)) : 0;
+  const size_t total = keys_b + misc_b + x_b + pkg_b;
   void *base = nullptr;
   e = cudaMalloc(&base, total);
   if (e != cudaSuccess) {
@@ -149,6 +161,7 @@ int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k, i
   h->ws.ticket = reinterpret_cast<unsigned int *>(p + keys_b);
   h->ws.status = reinterpret_cast<uint32_t *>(p + keys_b + 16);
   h->ws.x = reinterpret_cast<float *>(p + keys_b + misc_b);
+  h->ws.xpkg = pkg_b ? p + keys_b + misc_b + x_b : nullptr;
   *out = h;
   return MUSE_OK;
 }
@@ -216,14 +229,18 @@ int muse_lmhead_forward_host(muse_lmhead *h, const float *hidden_host, int batch
 int muse_lmhead_launches_per_forward(const muse_lmhead *h, int batch, int with_norm) {
   if (!h) return MUSE_ERR_NULL;
   if (batch < 1 || batch > h->max_batch) return MUSE_ERR_BATCH;
-  if (choose_path(h, batch) == Path::B1) return 1;
-  return with_norm ? 2 : 1;  // generic: RMSNorm pre-pass + GEMV
+  switch (choose_path(h, batch)) {
+    case Path::B1: return 1;
+    case Path::TensorCore: return 2;   // activation-package prep + tcgen05 kernel
+    default: return with_norm ? 2 : 1;  // generic: RMSNorm pre-pass + GEMV
+  }
 }
 
 const char *muse_lmhead_path_name(const muse_lmhead *h, int batch) {
   if (!h || batch < 1 || batch > h->max_batch) return nullptr;
   switch (choose_path(h, batch)) {
     case Path::B1: return "gemv_b1";
+    case Path::TensorCore: return "gemm_tc";
     default: return "gemv_generic";
   }
 }
