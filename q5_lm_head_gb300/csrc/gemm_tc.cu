@@ -6,10 +6,10 @@
 // 1. prep_x_kernel: one CTA per Q5_K block column kb.  Normalises the hidden
 //    rows and writes, per block, an "activation package" already in the
 //    tensor-core operand layout (K-major, 8-row x 16-byte core matrices):
-//      x_hi  [NM rows][256]  f16(x)
-//      x_lo  [NM rows][256]  f16(x - x_hi)     (x_hi + x_lo = x to ~2^-22)
-//      x_min [NM rows][16]   k < 8: f16 hi of S_s = sum of x over sub-block s,
-//                            k >= 8: its f16 remainder
+//      x     [2*NM rows][256]  rows 0..NM-1: f16(x); rows NM..2NM-1: f16(x - f16(x))
+//                              (the two rows of a batch row sum to x to ~2^-22)
+//      x_min [NM rows][16]     k < 8: f16 hi of S_s = sum of x over sub-block s,
+//                              k >= 8: its f16 remainder
 //    Rows >= batch are zero.
 //
 // 2. gemm_tc_kernel: a persistent CTA per SM works on pairs of 128-row tiles.
@@ -23,9 +23,11 @@
 //      Dmin[r][b] (tcgen05.ld) to accumulate
 //          raw[r][b] += d * D[r][b] - dmin * Dmin[r][b]
 //      which is sum_e (d*sc_s*q_e - dmin*m_s) * x[b][e] for the block.
-//    * MMA warp (one thread issues): per tile and block, 16 K-steps x (x_hi,
-//      x_lo) f16 MMAs with f32 accumulation into D (M = 128, N = NM) and one
-//      MMA A_min x x_min into Dmin; tcgen05.commit hands the tile back.
+//    * MMA warp (the whole warp runs the loop with warp-uniform operands, one
+//      elected lane issues): per tile and block, 16 K-steps of f16 MMAs with f32
+//      accumulation into D (M = 128, N = 2*NM: the x_hi and x_lo rows side by
+//      side) and one MMA A_min x x_min into Dmin; tcgen05.commit hands the tile
+//      back.
 //    Each warpgroup has one A buffer and one D pair in tensor memory.  One
 //    mbarrier pair per warpgroup paces everything: "A ready, D read" and
 //    "A consumed, D written".
@@ -45,26 +47,29 @@ namespace {
 constexpr int kTileRows = 128;               // M of one MMA and of one warpgroup's tile
 constexpr int kPairRows = 2 * kTileRows;     // rows per weight box
 constexpr int kWStageBytes = kPairRows * kBlockBytes;   // 45,056
-constexpr int kWStages = 3;
 constexpr int kXStages = 2;
-constexpr int kThreads = 320;                // 2 warpgroups + producer warp + MMA warp
-constexpr int kProducerWarp = 8;
+constexpr int kThreads = 352;                // 2 warpgroups + weight producer + MMA + package producer
+constexpr int kProducerWarp = 8;             // weight boxes
 constexpr int kMmaWarp = 9;
+constexpr int kPkgWarp = 10;                 // activation packages
 constexpr uint32_t kTmemCols = 512;
 
 template <int NM>
 struct TcCfg {
   static_assert(NM == 16 || NM == 32, "MMA N");
-  static constexpr int kTileBytes = NM * kBlockWeights * 2;      // one f16 [NM][256] operand tile
-  static constexpr int kMinBytes = NM * 16 * 2;                  // [NM][16] f16
-  static constexpr int kPkgBytes = 2 * kTileBytes + kMinBytes;   // per block
+  static constexpr int kXRows = 2 * NM;                           // x_hi rows, then x_lo rows
+  static constexpr int kXBytes = kXRows * kBlockWeights * 2;      // f16 [2NM][256] operand tile
+  static constexpr int kMinBytes = NM * 16 * 2;                   // [NM][16] f16
+  static constexpr int kPkgBytes = kXBytes + kMinBytes;           // per block
+  static constexpr int kWStages = NM == 16 ? 4 : 3;               // as many weight stages as fit
   static constexpr int kSmemBytes = kWStages * kWStageBytes + kXStages * kPkgBytes + 1024;
-  static constexpr uint32_t kIdesc = tc::idesc_f16_f32(kTileRows, NM);
-  // tensor-memory columns of warpgroup w: A [128], A_min [8], D [NM], Dmin [NM]
-  static constexpr uint32_t col_a(int w) { return 256u * w; }
-  static constexpr uint32_t col_amin(int w) { return 256u * w + 128u; }
-  static constexpr uint32_t col_d(int w) { return 256u * w + 160u; }
-  static constexpr uint32_t col_dmin(int w) { return 256u * w + 192u; }
+  static constexpr uint32_t kIdesc = tc::idesc_f16_f32(kTileRows, 2 * NM);
+  static constexpr uint32_t kIdescMin = tc::idesc_f16_f32(kTileRows, NM);
+  // tensor-memory columns of warpgroup w: A [128], A_min [8], D [2NM], Dmin [NM]
+  __host__ __device__ static constexpr uint32_t col_a(int w) { return 256u * w; }
+  __host__ __device__ static constexpr uint32_t col_amin(int w) { return 256u * w + 128u; }
+  __host__ __device__ static constexpr uint32_t col_d(int w) { return 256u * w + 160u; }
+  __host__ __device__ static constexpr uint32_t col_dmin(int w) { return 256u * w + 224u; }
 };
 
 // Byte offset of element (n, k) in a K-major operand tile of `rows` rows
@@ -118,15 +123,15 @@ __global__ void __launch_bounds__(256)
                              : hidden[static_cast<size_t>(b) * k + col];
     const __half hi = __float2half_rn(x);
     const __half lo = __float2half_rn(x - __half2float(hi));
-    *reinterpret_cast<__half *>(pkg + kmajor_offset(NM, b, j)) = hi;
-    *reinterpret_cast<__half *>(pkg + C::kTileBytes + kmajor_offset(NM, b, j)) = lo;
+    *reinterpret_cast<__half *>(pkg + kmajor_offset(C::kXRows, b, j)) = hi;
+    *reinterpret_cast<__half *>(pkg + kmajor_offset(C::kXRows, NM + b, j)) = lo;
     float s = x;                            // sum over the 32 columns of sub-block `warp`
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) {
       const __half shi = __float2half_rn(s);
       const __half slo = __float2half_rn(s - __half2float(shi));
-      *reinterpret_cast<__half *>(pkg + 2 * C::kTileBytes + kmajor_offset(NM, b, warp)) = shi;
-      *reinterpret_cast<__half *>(pkg + 2 * C::kTileBytes + kmajor_offset(NM, b, 8 + warp)) = slo;
+      *reinterpret_cast<__half *>(pkg + C::kXBytes + kmajor_offset(NM, b, warp)) = shi;
+      *reinterpret_cast<__half *>(pkg + C::kXBytes + kmajor_offset(NM, b, 8 + warp)) = slo;
     }
   }
 }
@@ -227,11 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status) {
   using C = TcCfg<NM>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t *wst = smem;                                            // [kWStages][256 rows][176 B]
-  uint8_t *xst = smem + kWStages * kWStageBytes;                  // [kXStages][package]
+  uint8_t *wst = smem;                                            // [C::kWStages][256 rows][176 B]
+  uint8_t *xst = smem + C::kWStages * kWStageBytes;                  // [kXStages][package]
   uint64_t *bars = reinterpret_cast<uint64_t *>(xst + kXStages * C::kPkgBytes);
-  uint64_t *wfull = bars, *wempty = bars + kWStages;
-  uint64_t *xfull = wempty + kWStages, *xempty = xfull + kXStages;
+  uint64_t *wfull = bars, *wempty = bars + C::kWStages;
+  uint64_t *xfull = wempty + C::kWStages, *xempty = xfull + kXStages;
   uint64_t *aready = xempty + kXStages;                           // [2]: A written, D read
   uint64_t *adone = aready + 2;                                   // [2]: MMAs of the block complete
   uint64_t *mma_idle = adone + 2;                                 // all MMAs of this CTA complete
@@ -246,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t total = my_pairs * nb;                            // (pair, block) steps of this CTA
 
   if (tid == 0) {
-    for (int s = 0; s < kWStages; ++s) {
+    for (int s = 0; s < C::kWStages; ++s) {
       ptx::mbar_init(&wfull[s], 1);
       ptx::mbar_init(&wempty[s], 8);                              // the eight unpack warps
     }
@@ -278,20 +283,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ weight producer
     if (lane == 0) {
       const uint64_t pol_w = ptx::policy_evict_first();
-      int64_t issued_w = 0, issued_x = 0;
+      int64_t issued = 0;
       for (int64_t g = 0; g < total && !*s_abort; ++g) {
         const int64_t pair = blockIdx.x + (g / nb) * gridDim.x;
         const int kb = static_cast<int>(g % nb);
-        const int ws = static_cast<int>(g % kWStages), xs = static_cast<int>(g % kXStages);
-        if (g >= kWStages &&
-            !ptx::mbar_wait(&wempty[ws], static_cast<uint32_t>((g / kWStages - 1) & 1))) { fail(); break; }
+        const int ws = static_cast<int>(g % C::kWStages);
+        if (g >= C::kWStages &&
+            !ptx::mbar_wait(&wempty[ws], static_cast<uint32_t>((g / C::kWStages - 1) & 1))) { fail(); break; }
         ptx::mbar_arrive_expect_tx(&wfull[ws], kWStageBytes);
         tma_load_2d(wst + ws * kWStageBytes, &wmap, kb * (kBlockBytes / 4), static_cast<int>(pair * kPairRows),
                     &wfull[ws], pol_w);
-        issued_w = g + 1;
+        issued = g + 1;
+      }
+      // never leave copies in flight
+      for (int64_t g = issued > C::kWStages ? issued - C::kWStages : 0; g < issued; ++g)
+        ptx::mbar_wait(&wfull[g % C::kWStages], static_cast<uint32_t>((g / C::kWStages) & 1));
+    }
+  } else if (warp == kPkgWarp) {
+    // ------------------------------------------------------------ activation-package producer
+    if (lane == 0) {
+      int64_t issued = 0;
+      for (int64_t g = 0; g < total && !*s_abort; ++g) {
+        const int kb = static_cast<int>(g % nb);
+        const int xs = static_cast<int>(g % kXStages);
         if (g >= kXStages &&
             !ptx::mbar_wait(&xempty[xs], static_cast<uint32_t>((g / kXStages - 1) & 1))) { fail(); break; }
         ptx::mbar_arrive_expect_tx(&xfull[xs], C::kPkgBytes);
@@ -300,46 +317,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                      "l"(pkgs + static_cast<size_t>(kb) * C::kPkgBytes), "r"(C::kPkgBytes),
                      "r"(ptx::smem_u32(&xfull[xs]))
                      : "memory");
-        issued_x = g + 1;
+        issued = g + 1;
       }
-      // never leave copies in flight
-      for (int64_t g = issued_w > kWStages ? issued_w - kWStages : 0; g < issued_w; ++g)
-        ptx::mbar_wait(&wfull[g % kWStages], static_cast<uint32_t>((g / kWStages) & 1));
-      for (int64_t g = issued_x > kXStages ? issued_x - kXStages : 0; g < issued_x; ++g)
+      for (int64_t g = issued > kXStages ? issued - kXStages : 0; g < issued; ++g)
         ptx::mbar_wait(&xfull[g % kXStages], static_cast<uint32_t>((g / kXStages) & 1));
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      for (int64_t g = 0; g < total && !*s_abort; ++g) {
-        const int xs = static_cast<int>(g % kXStages);
-        const uint32_t par = static_cast<uint32_t>(g & 1);
-        if (!ptx::mbar_wait(&xfull[xs], static_cast<uint32_t>((g / kXStages) & 1))) { fail(); break; }
-        const uint32_t xbase = ptx::smem_u32(xst + xs * C::kPkgBytes);
-        bool ok = true;
-        for (int w = 0; w < 2 && ok; ++w) {
-          if (!ptx::mbar_wait(&aready[w], par)) { ok = false; break; }
-          tc::fence_after();
-          const uint32_t d = tc::taddr(tbase, 0, C::col_d(w));
-#pragma unroll 4
-          for (int ks = 0; ks < 16; ++ks) {
-            const uint32_t a = tc::taddr(tbase, 0, C::col_a(w) + 8 * ks);
-            const uint32_t off = 2 * ks * (NM / 8) * 128;
-            tc::mma_f16_tmemA(d, a, tc::smem_desc_kmajor(xbase + off, NM * 16, 128), C::kIdesc, ks > 0);
-            tc::mma_f16_tmemA(d, a, tc::smem_desc_kmajor(xbase + C::kTileBytes + off, NM * 16, 128), C::kIdesc,
-                              true);
-          }
-          tc::mma_f16_tmemA(tc::taddr(tbase, 0, C::col_dmin(w)), tc::taddr(tbase, 0, C::col_amin(w)),
-                            tc::smem_desc_kmajor(xbase + 2 * C::kTileBytes, NM * 16, 128), C::kIdesc, false);
+    // The whole warp runs this loop (waits and operands stay warp-uniform); one
+    // elected lane issues the MMAs and commits.
+    bool ok = true;
+    for (int64_t g = 0; g < total && ok; ++g) {
+      if (__any_sync(0xffffffffu, *s_abort != 0u)) break;
+      const int xs = static_cast<int>(g % kXStages);
+      const uint32_t par = static_cast<uint32_t>(g & 1);
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&xfull[xs], static_cast<uint32_t>((g / kXStages) & 1)))) {
+        ok = false;
+        break;
+      }
+      const uint32_t xbase = ptx::smem_u32(xst + xs * C::kPkgBytes);
+      const uint64_t bdesc0 = tc::smem_desc_kmajor(xbase, C::kXRows * 16, 128);
+      const uint64_t mdesc = tc::smem_desc_kmajor(xbase + C::kXBytes, NM * 16, 128);
+      for (int w = 0; w < 2; ++w) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&aready[w], par))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        if (tc::elect_one()) {
+          const uint32_t d = tbase + C::col_d(w);
+          const uint32_t a = tbase + C::col_a(w);
+#pragma unroll
+          for (int ks = 0; ks < 16; ++ks)   // K-step ks: 16 columns of x = 2 core matrices along K
+            tc::mma_f16_tmemA(d, a + 8 * ks, bdesc0 + ((ks * 2 * (C::kXRows / 8) * 128) >> 4), C::kIdesc, ks > 0);
+          tc::mma_f16_tmemA(tbase + C::col_dmin(w), tbase + C::col_amin(w), mdesc, C::kIdescMin, false);
           tc::commit(&adone[w]);
         }
-        if (!ok) { fail(); break; }
-        tc::commit(&xempty[xs]);
+        __syncwarp();
       }
-      // tensor memory is freed below only after every MMA issued here completed
-      tc::commit(mma_idle);
-      if (!ptx::mbar_wait(mma_idle, 0)) fail();
+      if (!ok) break;
+      if (tc::elect_one()) tc::commit(&xempty[xs]);
+      __syncwarp();
     }
+    if (!ok && lane == 0) fail();
+    // tensor memory is freed below only after every MMA issued here completed
+    if (tc::elect_one()) tc::commit(mma_idle);
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, ptx::mbar_wait(mma_idle, 0)) && lane == 0) fail();
   } else {
     // ------------------------------------------------------------ unpack + epilogue (warpgroup w)
     const int w = warp >> 2;                    // 0 or 1: which tile of the pair
@@ -371,13 +395,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < NM; c0 += 16) {
-        uint32_t dv[16], mv[16];
-        tc::ld_32x32b_x16(tbase + lane_base + C::col_d(w) + c0, dv);
+        uint32_t dh[16], dl[16], mv[16];
+        tc::ld_32x32b_x16(tbase + lane_base + C::col_d(w) + c0, dh);        // x_hi columns
+        tc::ld_32x32b_x16(tbase + lane_base + C::col_d(w) + NM + c0, dl);   // x_lo columns
         tc::ld_32x32b_x16(tbase + lane_base + C::col_dmin(w) + c0, mv);
         tc::wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          acc[c0 + j] = fmaf(d_prev, __uint_as_float(dv[j]), fmaf(-dmin_prev, __uint_as_float(mv[j]), acc[c0 + j]));
+        for (int j = 0; j < 16; ++j) {
+          const float dot = __uint_as_float(dh[j]) + __uint_as_float(dl[j]);
+          acc[c0 + j] = fmaf(d_prev, dot, fmaf(-dmin_prev, __uint_as_float(mv[j]), acc[c0 + j]));
+        }
       }
     };
     bool ok_all = true;
@@ -385,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__any_sync(0xffffffffu, *s_abort != 0u)) { ok_all = false; break; }
       const int64_t pair = blockIdx.x + (g / nb) * gridDim.x;
       const int kb = static_cast<int>(g % nb);
-      const int ws = static_cast<int>(g % kWStages);
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wfull[ws], static_cast<uint32_t>((g / kWStages) & 1)))) {
+      const int ws = static_cast<int>(g % C::kWStages);
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wfull[ws], static_cast<uint32_t>((g / C::kWStages) & 1)))) {
         if (lane == 0) fail();
         ok_all = false;
         break;

@@ -105,6 +105,17 @@ __device__ __forceinline__ void mma_f16_tmemA(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// One lane of a converged warp returns true (elect.sync).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // The mbarrier receives one arrival when every tcgen05 operation this thread
 // issued before the commit has completed.
 __device__ __forceinline__ void commit(uint64_t *bar) {
