@@ -8,30 +8,34 @@
 //    tensor-core operand layout (K-major, 8-row x 16-byte core matrices):
 //      x     [2*NM rows][256]  rows 0..NM-1: f16(x); rows NM..2NM-1: f16(x - f16(x))
 //                              (the two rows of a batch row sum to x to ~2^-22)
-//      x_min [NM rows][16]     k < 8: f16 hi of S_s = sum of x over sub-block s,
-//                              k >= 8: its f16 remainder
+//      x_min [max(NM,16) rows][16]  k < 8: f16 hi of S_s = sum of x over
+//                              sub-block s, k >= 8: its f16 remainder
 //    Rows >= batch are zero.
 //
-// 2. gemm_tc_kernel: a persistent CTA per SM works on pairs of 128-row tiles.
-//    * producer warp: per block kb, one 2-D TMA box of 256 rows x 176 bytes
-//      (both tiles of the pair) into a ring of weight stages, and the kb
+// 2. gemm_tc_kernel: a persistent CTA per SM works on 128-row tiles.
+//    * weight producer warp: per block kb, one 2-D TMA box of 128 rows x 176
+//      bytes into a ring of weight stages.  Package producer warp: the kb
 //      activation package (1-D bulk copy) into a ring of package stages.
-//    * two unpack warpgroups, one per tile: thread r owns row r.  It turns its
-//      row's block into A[r][e] = sc_s * q_e as f16 (exact: at most 31*63) and
-//      A_min[r][k] = m_(k mod 8), stores them into tensor memory
-//      (tcgen05.st), and after the block's MMAs reads back D[r][b] and
-//      Dmin[r][b] (tcgen05.ld) to accumulate
+//    * four unpack warpgroups in two pairs; pair p takes the blocks whose step
+//      index has parity p, so the two pairs work on consecutive blocks at once
+//      with their own tensor-memory buffers.  In a pair, thread r of either
+//      warpgroup owns row r: one warpgroup sub-blocks 0..3 and batch columns
+//      0..NM/2-1, the other sub-blocks 4..7 and the remaining columns.  A thread
+//      turns its half of the row's block into A[r][e] = sc_s * q_e as f16 (exact:
+//      at most 31*63) (the first warpgroup also A_min[r][k] = m_(k mod 8)),
+//      stores it into tensor memory (tcgen05.st), and after that block's MMAs
+//      reads back its columns of D[r][b] and Dmin[r][b] (tcgen05.ld) to
+//      accumulate
 //          raw[r][b] += d * D[r][b] - dmin * Dmin[r][b]
-//      which is sum_e (d*sc_s*q_e - dmin*m_s) * x[b][e] for the block.
+//      which is sum_e (d*sc_s*q_e - dmin*m_s) * x[b][e] for the block.  At the
+//      end of a tile the two pairs add their sums through shared memory and the
+//      first pair applies scale and soft cap, stores the logits and keeps the
+//      per-batch-row argmax keys.
 //    * MMA warp (the whole warp runs the loop with warp-uniform operands, one
-//      elected lane issues): per tile and block, 16 K-steps of f16 MMAs with f32
+//      elected lane issues): per block, 16 K-steps of f16 MMAs with f32
 //      accumulation into D (M = 128, N = 2*NM: the x_hi and x_lo rows side by
-//      side) and one MMA A_min x x_min into Dmin; tcgen05.commit hands the tile
-//      back.
-//    Each warpgroup has one A buffer and one D pair in tensor memory.  One
-//    mbarrier pair per warpgroup paces everything: "A ready, D read" and
-//    "A consumed, D written".
-//    Epilogue per tile: scale, soft cap, store logits, per-batch-row argmax key.
+//      side) and one MMA A_min x x_min into Dmin; tcgen05.commit hands the
+//      buffer back.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -44,32 +48,41 @@
 namespace muse {
 namespace {
 
-constexpr int kTileRows = 128;               // M of one MMA and of one warpgroup's tile
-constexpr int kPairRows = 2 * kTileRows;     // rows per weight box
-constexpr int kWStageBytes = kPairRows * kBlockBytes;   // 45,056
+constexpr int kTileRows = 128;                          // M of one MMA
+constexpr int kWStageBytes = kTileRows * kBlockBytes;   // 22,528: one block of a tile
 constexpr int kXStages = 2;
-constexpr int kThreads = 352;                // 2 warpgroups + weight producer + MMA + package producer
-constexpr int kProducerWarp = 8;             // weight boxes
-constexpr int kMmaWarp = 9;
-constexpr int kPkgWarp = 10;                 // activation packages
+constexpr int kUnpackWarps = 16;                        // 2 pairs x 2 warpgroups
+constexpr int kThreads = 32 * (kUnpackWarps + 3);       // + weight producer, MMA issuer, package producer
+constexpr int kProducerWarp = kUnpackWarps;
+constexpr int kMmaWarp = kUnpackWarps + 1;
+constexpr int kPkgWarp = kUnpackWarps + 2;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemLimit = 227 * 1024 - 1024;           // opt-in limit minus static shared memory
+
+// The min MMA needs N >= 16; for NM = 8 its operand tile has 16 rows, 8..15 zero.
+template <int NM>
+__host__ __device__ constexpr int min_rows() { return NM < 16 ? 16 : NM; }
 
 template <int NM>
 struct TcCfg {
-  static_assert(NM == 16 || NM == 32, "MMA N");
+  static_assert(NM == 8 || NM == 16 || NM == 32, "MMA N / 2");
   static constexpr int kXRows = 2 * NM;                           // x_hi rows, then x_lo rows
   static constexpr int kXBytes = kXRows * kBlockWeights * 2;      // f16 [2NM][256] operand tile
-  static constexpr int kMinBytes = NM * 16 * 2;                   // [NM][16] f16
+  static constexpr int kMinBytes = min_rows<NM>() * 16 * 2;       // f16 [rows][16]
   static constexpr int kPkgBytes = kXBytes + kMinBytes;           // per block
-  static constexpr int kWStages = NM == 16 ? 4 : 3;               // as many weight stages as fit
-  static constexpr int kSmemBytes = kWStages * kWStageBytes + kXStages * kPkgBytes + 1024;
+  static constexpr int kXchgBytes = 2 * kTileRows * (NM / 2) * 4; // pair-1 sums handed to pair 0
+  static constexpr int kFixed = kXStages * kPkgBytes + kXchgBytes + 1024;
+  static constexpr int kWFit = (kSmemLimit - kFixed) / kWStageBytes;
+  static constexpr int kWStages = (kWFit > 8 ? 8 : kWFit) & ~1;   // even: a stage always serves one pair
+  static_assert(kWStages >= 4, "weight ring");
+  static constexpr int kSmemBytes = kWStages * kWStageBytes + kFixed;
   static constexpr uint32_t kIdesc = tc::idesc_f16_f32(kTileRows, 2 * NM);
-  static constexpr uint32_t kIdescMin = tc::idesc_f16_f32(kTileRows, NM);
-  // tensor-memory columns of warpgroup w: A [128], A_min [8], D [2NM], Dmin [NM]
-  __host__ __device__ static constexpr uint32_t col_a(int w) { return 256u * w; }
-  __host__ __device__ static constexpr uint32_t col_amin(int w) { return 256u * w + 128u; }
-  __host__ __device__ static constexpr uint32_t col_d(int w) { return 256u * w + 160u; }
-  __host__ __device__ static constexpr uint32_t col_dmin(int w) { return 256u * w + 224u; }
+  static constexpr uint32_t kIdescMin = tc::idesc_f16_f32(kTileRows, min_rows<NM>());
+  // tensor-memory columns of buffer j: A [128], A_min [8], D [2NM], Dmin [max(NM,16)]
+  __host__ __device__ static constexpr uint32_t col_a(int j) { return 128u * j; }
+  __host__ __device__ static constexpr uint32_t col_amin(int j) { return 256u + 8u * j; }
+  __host__ __device__ static constexpr uint32_t col_d(int j) { return 288u + 96u * j; }
+  __host__ __device__ static constexpr uint32_t col_dmin(int j) { return 288u + 96u * j + 64u; }
 };
 
 // Byte offset of element (n, k) in a K-major operand tile of `rows` rows
@@ -117,26 +130,28 @@ __global__ void __launch_bounds__(256)
   const int j = tid;                        // column inside the block; warp = sub-block
   const int col = kb * kBlockWeights + j;
   const float g = gamma ? gamma[col] : 1.0f;
-  for (int b = 0; b < NM; ++b) {
+  for (int b = 0; b < min_rows<NM>(); ++b) {
     float x = 0.0f;
     if (b < batch) x = gamma ? hidden[static_cast<size_t>(b) * k + col] * s_r[b] * g
                              : hidden[static_cast<size_t>(b) * k + col];
-    const __half hi = __float2half_rn(x);
-    const __half lo = __float2half_rn(x - __half2float(hi));
-    *reinterpret_cast<__half *>(pkg + kmajor_offset(C::kXRows, b, j)) = hi;
-    *reinterpret_cast<__half *>(pkg + kmajor_offset(C::kXRows, NM + b, j)) = lo;
+    if (b < NM) {
+      const __half hi = __float2half_rn(x);
+      const __half lo = __float2half_rn(x - __half2float(hi));
+      *reinterpret_cast<__half *>(pkg + kmajor_offset(C::kXRows, b, j)) = hi;
+      *reinterpret_cast<__half *>(pkg + kmajor_offset(C::kXRows, NM + b, j)) = lo;
+    }
     float s = x;                            // sum over the 32 columns of sub-block `warp`
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) {
       const __half shi = __float2half_rn(s);
       const __half slo = __float2half_rn(s - __half2float(shi));
-      *reinterpret_cast<__half *>(pkg + C::kXBytes + kmajor_offset(NM, b, warp)) = shi;
-      *reinterpret_cast<__half *>(pkg + C::kXBytes + kmajor_offset(NM, b, 8 + warp)) = slo;
+      *reinterpret_cast<__half *>(pkg + C::kXBytes + kmajor_offset(min_rows<NM>(), b, warp)) = shi;
+      *reinterpret_cast<__half *>(pkg + C::kXBytes + kmajor_offset(min_rows<NM>(), b, 8 + warp)) = slo;
     }
   }
 }
 
-// ------------------------------------------------------------------ main kernel
+// ------------------------------------------------------------------ unpack helpers
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
                                             uint64_t policy) {
   asm volatile(
@@ -171,15 +186,10 @@ __device__ __forceinline__ uint32_t h2_bits(float v) {
 struct RowHdr {
   float d, dmin;
   uint32_t sc03, sc47, m03, m47;
-  uint32_t H[8];
 };
 
 __device__ __forceinline__ void load_row_hdr(const uint8_t *blk, RowHdr &o) {
   const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-  const uint4 h0 = *reinterpret_cast<const uint4 *>(blk + kOffQh);
-  const uint4 h1 = *reinterpret_cast<const uint4 *>(blk + kOffQh + 16);
-  o.H[0] = h0.x; o.H[1] = h0.y; o.H[2] = h0.z; o.H[3] = h0.w;
-  o.H[4] = h1.x; o.H[5] = h1.y; o.H[6] = h1.z; o.H[7] = h1.w;
   const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));
   o.d = dd.x;
   o.dmin = dd.y;
@@ -200,70 +210,96 @@ __device__ __forceinline__ void amin_cols(const RowHdr &h, uint32_t (&o)[8]) {
 }
 
 // Columns 32c..32c+31 of A for one row: sub-blocks 2c (low nibbles, built as q)
-// and 2c+1 (high nibbles, built as 2q), as f16 pairs sc_s*q in natural K order.
-template <int C>
-__device__ __forceinline__ void a_chunk(const uint8_t *blk, const RowHdr &h, uint32_t (&o)[32]) {
-  const uint32_t scw = C < 2 ? h.sc03 : h.sc47;
-  constexpr int sh = 16 * (C & 1);
+// and 2c+1 (high nibbles, built as 2q), as f16 pairs sc_s*q in natural K order;
+// stored to tensor memory at column `ta` in two 16-column halves.
+__device__ __forceinline__ void a_chunk_st(const uint8_t *blk, const RowHdr &h, int c, uint32_t ta) {
+  const uint32_t scw = c < 2 ? h.sc03 : h.sc47;
+  const uint32_t sh = 16u * (c & 1);
   const float sc_lo = static_cast<float>((scw >> sh) & 0xFFu);
   const float sc_hi = static_cast<float>((scw >> (sh + 8)) & 0xFFu);
-  const uint32_t mul_lo = h2_bits(sc_lo), add_lo = h2_bits(-1024.0f * sc_lo);
-  const uint32_t mul_hi = h2_bits(0.5f * sc_hi), add_hi = h2_bits(-512.0f * sc_hi);
-  const uint4 a0 = *reinterpret_cast<const uint4 *>(blk + kOffQs + 32 * C);
-  const uint4 a1 = *reinterpret_cast<const uint4 *>(blk + kOffQs + 32 * C + 16);
+  const uint4 a0 = *reinterpret_cast<const uint4 *>(blk + kOffQs + 32 * c);
+  const uint4 a1 = *reinterpret_cast<const uint4 *>(blk + kOffQs + 32 * c + 16);
   const uint32_t A[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-  constexpr uint32_t rot = static_cast<uint32_t>(4 - 2 * C) & 31u;   // bit 2C -> 4, bit 2C+1 -> 5
+  const uint4 h0 = *reinterpret_cast<const uint4 *>(blk + kOffQh);
+  const uint4 h1 = *reinterpret_cast<const uint4 *>(blk + kOffQh + 16);
+  uint32_t H[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+  const uint32_t rot = static_cast<uint32_t>(4 - 2 * c) & 31u;   // bit 2c -> 4, bit 2c+1 -> 5
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t t = rotl32(h.H[i], rot);
-    const uint32_t qlo = (A[i] & 0x0F0F0F0Fu) | (t & 0x10101010u);        // q, positions 4i..4i+3
-    const uint32_t qhi = ((A[i] >> 3) & 0x1E1E1E1Eu) | (t & 0x20202020u);  // 2q
-    o[2 * i] = hfma2_u32(magic_pair<0>(qlo), mul_lo, add_lo);
-    o[2 * i + 1] = hfma2_u32(magic_pair<2>(qlo), mul_lo, add_lo);
-    o[16 + 2 * i] = hfma2_u32(magic_pair<0>(qhi), mul_hi, add_hi);
-    o[16 + 2 * i + 1] = hfma2_u32(magic_pair<2>(qhi), mul_hi, add_hi);
+  for (int i = 0; i < 8; ++i) H[i] = rotl32(H[i], rot);
+  uint32_t o[16];
+  {
+    const uint32_t mul = h2_bits(sc_lo), add = h2_bits(-1024.0f * sc_lo);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t q = (A[i] & 0x0F0F0F0Fu) | (H[i] & 0x10101010u);          // q, positions 4i..4i+3
+      o[2 * i] = hfma2_u32(magic_pair<0>(q), mul, add);
+      o[2 * i + 1] = hfma2_u32(magic_pair<2>(q), mul, add);
+    }
+    tc::st_32x32b_x16(ta, o);
+  }
+  {
+    const uint32_t mul = h2_bits(0.5f * sc_hi), add = h2_bits(-512.0f * sc_hi);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t q = ((A[i] >> 3) & 0x1E1E1E1Eu) | (H[i] & 0x20202020u);   // 2q
+      o[2 * i] = hfma2_u32(magic_pair<0>(q), mul, add);
+      o[2 * i + 1] = hfma2_u32(magic_pair<2>(q), mul, add);
+    }
+    tc::st_32x32b_x16(ta + 16, o);
   }
 }
 
+__device__ __forceinline__ void ld_x4(uint32_t ta, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(ta)
+               : "memory");
+}
+
+// ------------------------------------------------------------------ main kernel
 template <int NM>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const uint8_t *__restrict__ pkgs, int nb,
                    int64_t n_rows, int batch, float scale, float cap, float *__restrict__ logits,
                    unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status) {
   using C = TcCfg<NM>;
+  constexpr int HB = NM / 2;                                      // batch columns per warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t *wst = smem;                                            // [C::kWStages][256 rows][176 B]
-  uint8_t *xst = smem + C::kWStages * kWStageBytes;                  // [kXStages][package]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(xst + kXStages * C::kPkgBytes);
+  uint8_t *wst = smem;                                            // [kWStages][128 rows][176 B]
+  uint8_t *xst = smem + C::kWStages * kWStageBytes;               // [kXStages][package]
+  float *xchg = reinterpret_cast<float *>(xst + kXStages * C::kPkgBytes);   // [2 halves][128][HB]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) + C::kXchgBytes);
   uint64_t *wfull = bars, *wempty = bars + C::kWStages;
   uint64_t *xfull = wempty + C::kWStages, *xempty = xfull + kXStages;
   uint64_t *aready = xempty + kXStages;                           // [2]: A written, D read
-  uint64_t *adone = aready + 2;                                   // [2]: MMAs of the block complete
+  uint64_t *adone = aready + 2;                                   // [2]: MMAs of the buffer complete
   uint64_t *mma_idle = adone + 2;                                 // all MMAs of this CTA complete
-  unsigned long long *s_keys = reinterpret_cast<unsigned long long *>(mma_idle + 1);   // [32]
+  uint64_t *xch_full = mma_idle + 1, *xch_empty = mma_idle + 2;   // tile-end hand-over, pair 1 -> pair 0
+  unsigned long long *s_keys = reinterpret_cast<unsigned long long *>(mma_idle + 3);   // [32]
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_keys + 32);
   volatile uint32_t *s_abort = s_tmem + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t n_tiles = (n_rows + kTileRows - 1) / kTileRows;
-  const int64_t n_pairs = (n_tiles + 1) / 2;
-  const int64_t my_pairs = blockIdx.x < n_pairs ? (n_pairs - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int64_t total = my_pairs * nb;                            // (pair, block) steps of this CTA
+  const int64_t my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int64_t total = my_tiles * nb;                            // (tile, block) steps of this CTA
 
   if (tid == 0) {
     for (int s = 0; s < C::kWStages; ++s) {
       ptx::mbar_init(&wfull[s], 1);
-      ptx::mbar_init(&wempty[s], 8);                              // the eight unpack warps
+      ptx::mbar_init(&wempty[s], 8);                              // the pair's eight warps
     }
     for (int s = 0; s < kXStages; ++s) {
       ptx::mbar_init(&xfull[s], 1);
-      ptx::mbar_init(&xempty[s], 1);                              // one commit after both tiles' MMAs
+      ptx::mbar_init(&xempty[s], 1);                              // one commit after the block's MMAs
     }
-    for (int w = 0; w < 2; ++w) {
-      ptx::mbar_init(&aready[w], 4);
-      ptx::mbar_init(&adone[w], 1);
+    for (int j = 0; j < 2; ++j) {
+      ptx::mbar_init(&aready[j], 8);
+      ptx::mbar_init(&adone[j], 1);
     }
     ptx::mbar_init(mma_idle, 1);
+    ptx::mbar_init(xch_full, 32 * kUnpackWarps / 2);
+    ptx::mbar_init(xch_empty, 32 * kUnpackWarps / 2);
     for (int b = 0; b < 32; ++b) s_keys[b] = 0ull;
     *s_abort = 0u;
     ptx::fence_barrier_init();
@@ -288,13 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = ptx::policy_evict_first();
       int64_t issued = 0;
       for (int64_t g = 0; g < total && !*s_abort; ++g) {
-        const int64_t pair = blockIdx.x + (g / nb) * gridDim.x;
+        const int64_t tile = blockIdx.x + (g / nb) * gridDim.x;
         const int kb = static_cast<int>(g % nb);
         const int ws = static_cast<int>(g % C::kWStages);
         if (g >= C::kWStages &&
             !ptx::mbar_wait(&wempty[ws], static_cast<uint32_t>((g / C::kWStages - 1) & 1))) { fail(); break; }
         ptx::mbar_arrive_expect_tx(&wfull[ws], kWStageBytes);
-        tma_load_2d(wst + ws * kWStageBytes, &wmap, kb * (kBlockBytes / 4), static_cast<int>(pair * kPairRows),
+        tma_load_2d(wst + ws * kWStageBytes, &wmap, kb * (kBlockBytes / 4), static_cast<int>(tile * kTileRows),
                     &wfull[ws], pol_w);
         issued = g + 1;
       }
@@ -327,36 +363,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs this loop (waits and operands stay warp-uniform); one
     // elected lane issues the MMAs and commits.
     bool ok = true;
-    for (int64_t g = 0; g < total && ok; ++g) {
+    for (int64_t g = 0; g < total; ++g) {
       if (__any_sync(0xffffffffu, *s_abort != 0u)) break;
       const int xs = static_cast<int>(g % kXStages);
-      const uint32_t par = static_cast<uint32_t>(g & 1);
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&xfull[xs], static_cast<uint32_t>((g / kXStages) & 1)))) {
-        ok = false;
-        break;
-      }
+      const int j = static_cast<int>(g & 1);
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&xfull[xs], static_cast<uint32_t>((g / kXStages) & 1)));
+      if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&aready[j], static_cast<uint32_t>((g >> 1) & 1)));
+      if (!ok) break;
+      tc::fence_after();
       const uint32_t xbase = ptx::smem_u32(xst + xs * C::kPkgBytes);
       const uint64_t bdesc0 = tc::smem_desc_kmajor(xbase, C::kXRows * 16, 128);
-      const uint64_t mdesc = tc::smem_desc_kmajor(xbase + C::kXBytes, NM * 16, 128);
-      for (int w = 0; w < 2; ++w) {
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&aready[w], par))) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
-        if (tc::elect_one()) {
-          const uint32_t d = tbase + C::col_d(w);
-          const uint32_t a = tbase + C::col_a(w);
+      const uint64_t mdesc = tc::smem_desc_kmajor(xbase + C::kXBytes, min_rows<NM>() * 16, 128);
+      if (tc::elect_one()) {
+        const uint32_t d = tbase + C::col_d(j);
+        const uint32_t a = tbase + C::col_a(j);
 #pragma unroll
-          for (int ks = 0; ks < 16; ++ks)   // K-step ks: 16 columns of x = 2 core matrices along K
-            tc::mma_f16_tmemA(d, a + 8 * ks, bdesc0 + ((ks * 2 * (C::kXRows / 8) * 128) >> 4), C::kIdesc, ks > 0);
-          tc::mma_f16_tmemA(tbase + C::col_dmin(w), tbase + C::col_amin(w), mdesc, C::kIdescMin, false);
-          tc::commit(&adone[w]);
-        }
-        __syncwarp();
+        for (int ks = 0; ks < 16; ++ks)   // K-step ks: 16 columns of x = 2 core matrices along K
+          tc::mma_f16_tmemA(d, a + 8 * ks, bdesc0 + ((ks * 2 * (C::kXRows / 8) * 128) >> 4), C::kIdesc, ks > 0);
+        tc::mma_f16_tmemA(tbase + C::col_dmin(j), tbase + C::col_amin(j), mdesc, C::kIdescMin, false);
+        tc::commit(&adone[j]);
+        tc::commit(&xempty[xs]);
       }
-      if (!ok) break;
-      if (tc::elect_one()) tc::commit(&xempty[xs]);
       __syncwarp();
     }
     if (!ok && lane == 0) fail();
@@ -365,98 +392,127 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (!__all_sync(0xffffffffu, ptx::mbar_wait(mma_idle, 0)) && lane == 0) fail();
   } else {
-    // ------------------------------------------------------------ unpack + epilogue (warpgroup w)
-    const int w = warp >> 2;                    // 0 or 1: which tile of the pair
+    // ------------------------------------------------------------ unpack + epilogue
+    const int wg = warp >> 2;                   // warpgroup 0..3
+    const int p = wg >> 1;                      // pair: steps of parity p, tensor-memory buffer p
+    const int hf = wg & 1;                      // half of the block (sub-blocks 4hf..4hf+3)
     const int r = tid & 127;                    // row inside the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    float acc[32];
+    const int b0 = hf * HB;
+    float acc[HB];
 #pragma unroll
-    for (int b = 0; b < 32; ++b) acc[b] = 0.0f;
+    for (int b = 0; b < HB; ++b) acc[b] = 0.0f;
     float d_prev = 0.0f, dmin_prev = 0.0f;
-    int64_t row_prev = -1;
-    auto finish_tile = [&](int64_t row) {      // scale, cap, store, argmax keys; reset accumulators
-#pragma unroll
-      for (int b = 0; b < 32; ++b) {
-        if (b < batch) {
-          const float v = scale_softcap(acc[b], scale, cap);
-          unsigned long long key = 0ull;
-          if (row < n_rows) {
-            logits[static_cast<size_t>(b) * n_rows + row] = v;
-            key = argmax_key(v, static_cast<uint32_t>(row));
-          }
-          for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xffffffffu, key, o));
-          if (lane == 0 && key != 0ull) atomicMax(&s_keys[b], key);
-        }
-        acc[b] = 0.0f;
-      }
-    };
-    // read back the previous block's D and Dmin (its MMAs are complete) and accumulate
+    // read back this warpgroup's columns of buffer p's D and Dmin (the pair's
+    // previous block: its MMAs are complete) and accumulate
     auto drain = [&]() {
       tc::fence_after();
+      const uint32_t cd = tbase + lane_base + C::col_d(p) + b0;
+      const uint32_t cm = tbase + lane_base + C::col_dmin(p) + b0;
 #pragma unroll
-      for (int c0 = 0; c0 < NM; c0 += 16) {
-        uint32_t dh[16], dl[16], mv[16];
-        tc::ld_32x32b_x16(tbase + lane_base + C::col_d(w) + c0, dh);        // x_hi columns
-        tc::ld_32x32b_x16(tbase + lane_base + C::col_d(w) + NM + c0, dl);   // x_lo columns
-        tc::ld_32x32b_x16(tbase + lane_base + C::col_dmin(w) + c0, mv);
+      for (int c0 = 0; c0 < HB; c0 += 4) {
+        uint32_t dh[4], dl[4], mv[4];
+        ld_x4(cd + c0, dh);          // x_hi columns
+        ld_x4(cd + NM + c0, dl);     // x_lo columns
+        ld_x4(cm + c0, mv);
         tc::wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float dot = __uint_as_float(dh[j]) + __uint_as_float(dl[j]);
-          acc[c0 + j] = fmaf(d_prev, dot, fmaf(-dmin_prev, __uint_as_float(mv[j]), acc[c0 + j]));
+        for (int q = 0; q < 4; ++q) {
+          const float dot = __uint_as_float(dh[q]) + __uint_as_float(dl[q]);
+          acc[c0 + q] = fmaf(d_prev, dot, fmaf(-dmin_prev, __uint_as_float(mv[q]), acc[c0 + q]));
         }
       }
     };
+    // End of a tile: pair 1 hands its sums to pair 0 through shared memory
+    // (bounded mbarrier handshake), pair 0 finishes the rows.
+    uint32_t n_fin = 0;
+    auto finish_tile = [&](int64_t row) -> bool {
+      float *xw = xchg + (hf * kTileRows + r) * HB;
+      bool ok = true;
+      if (p == 1) {
+        if (n_fin > 0) ok = __all_sync(0xffffffffu, ptx::mbar_wait(xch_empty, (n_fin - 1) & 1u));
+        if (ok) {
+#pragma unroll
+          for (int b = 0; b < HB; ++b) xw[b] = acc[b];
+          ptx::mbar_arrive(xch_full);
+        }
+      } else {
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(xch_full, n_fin & 1u));
+        if (ok) {
+#pragma unroll
+          for (int b = 0; b < HB; ++b) {
+            if (b0 + b < batch) {
+              const float v = scale_softcap(acc[b] + xw[b], scale, cap);
+              unsigned long long key = 0ull;
+              if (row < n_rows) {
+                logits[static_cast<size_t>(b0 + b) * n_rows + row] = v;
+                key = argmax_key(v, static_cast<uint32_t>(row));
+              }
+              for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xffffffffu, key, o));
+              if (lane == 0 && key != 0ull) atomicMax(&s_keys[b0 + b], key);
+            }
+          }
+          ptx::mbar_arrive(xch_empty);
+        }
+      }
+      ++n_fin;
+#pragma unroll
+      for (int b = 0; b < HB; ++b) acc[b] = 0.0f;
+      return ok;
+    };
     bool ok_all = true;
-    for (int64_t g = 0; g < total; ++g) {
+    int64_t tile_prev = -1;
+    for (int64_t g = p; g < total; g += 2) {
       if (__any_sync(0xffffffffu, *s_abort != 0u)) { ok_all = false; break; }
-      const int64_t pair = blockIdx.x + (g / nb) * gridDim.x;
-      const int kb = static_cast<int>(g % nb);
+      const int64_t tile = blockIdx.x + (g / nb) * gridDim.x;
       const int ws = static_cast<int>(g % C::kWStages);
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wfull[ws], static_cast<uint32_t>((g / C::kWStages) & 1)))) {
         if (lane == 0) fail();
         ok_all = false;
         break;
       }
-      const uint8_t *blk = wst + ws * kWStageBytes + (w * kTileRows + r) * kBlockBytes;
+      const uint8_t *blk = wst + ws * kWStageBytes + r * kBlockBytes;
       RowHdr hd;
       load_row_hdr(blk, hd);
-      uint32_t c0[32], c1[32];
-      a_chunk<0>(blk, hd, c0);                  // overlaps the previous block's MMAs
-      a_chunk<1>(blk, hd, c1);
-      if (g >= 1) {                             // the previous block's MMAs: A consumed, D written
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&adone[w], static_cast<uint32_t>((g - 1) & 1)))) {
+      const uint32_t ta = tbase + lane_base + C::col_a(p) + 64 * hf;
+      if (g >= 2) {                             // buffer p: previous block's A consumed, D written
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&adone[p], static_cast<uint32_t>(((g - 2) >> 1) & 1)))) {
           if (lane == 0) fail();
           ok_all = false;
           break;
         }
         drain();
-        if (kb == 0) finish_tile(row_prev);     // the previous block closed the previous tile
+        if (tile != tile_prev && !finish_tile(tile_prev * kTileRows + r)) {   // that block closed a tile
+          if (lane == 0) fail();
+          ok_all = false;
+          break;
+        }
       }
-      const uint32_t ta = tbase + lane_base + C::col_a(w);
-      tc::st_32x32b_x32(ta, c0);
-      tc::st_32x32b_x32(ta + 32, c1);
-      a_chunk<2>(blk, hd, c0);
-      tc::st_32x32b_x32(ta + 64, c0);
-      a_chunk<3>(blk, hd, c1);
-      tc::st_32x32b_x32(ta + 96, c1);
-      uint32_t am[8];
-      amin_cols(hd, am);
-      tc::st_32x32b_x8(tbase + lane_base + C::col_amin(w), am);
+      a_chunk_st(blk, hd, 2 * hf, ta);
+      a_chunk_st(blk, hd, 2 * hf + 1, ta + 32);
+      if (hf == 0) {
+        uint32_t am[8];
+        amin_cols(hd, am);
+        tc::st_32x32b_x8(tbase + lane_base + C::col_amin(p), am);
+      }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&wempty[ws]);   // weight stage fully read
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&aready[w]);
+      if (lane == 0) ptx::mbar_arrive(&aready[p]);
       d_prev = hd.d;
       dmin_prev = hd.dmin;
-      row_prev = (pair * 2 + w) * kTileRows + r;
+      tile_prev = tile;
     }
-    if (ok_all && total > 0) {
-      if (__all_sync(0xffffffffu, ptx::mbar_wait(&adone[w], static_cast<uint32_t>((total - 1) & 1)))) {
+    // The pair's last block and the last tile.  Both pairs get here having
+    // taken part in the same tile hand-overs: nb is even, so each pair owns
+    // blocks of every tile.
+    if (ok_all && tile_prev >= 0) {
+      const int64_t g_last = p + ((total - 1 - p) / 2) * 2;
+      if (__all_sync(0xffffffffu, ptx::mbar_wait(&adone[p], static_cast<uint32_t>((g_last >> 1) & 1)))) {
         drain();
-        finish_tile(row_prev);
+        if (!finish_tile(tile_prev * kTileRows + r) && lane == 0) fail();
       } else if (lane == 0) {
         fail();
       }
@@ -507,8 +563,7 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t n_tiles = (a.n_rows + kTileRows - 1) / kTileRows;
-  const int64_t n_pairs = (n_tiles + 1) / 2;
-  const int64_t grid = n_pairs < a.num_sms ? n_pairs : a.num_sms;
+  const int64_t grid = n_tiles < a.num_sms ? n_tiles : a.num_sms;
   gemm_tc_kernel<NM><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(
       map, a.ws.xpkg, nb, a.n_rows, a.batch, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax,
       a.ws.status);
@@ -519,7 +574,12 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
 
 size_t tc_workspace_bytes(int k) { return static_cast<size_t>(k / kBlockWeights) * TcCfg<32>::kPkgBytes; }
 
-bool tc_supported(int batch) { return batch >= 2 && batch <= 32; }
+// Batches 2..32 with an even number of Q5_K blocks per row (both pairs of
+// unpack warpgroups then own blocks of every tile).
+bool tc_supported(int batch, int k) {
+  const int nb = k / kBlockWeights;
+  return batch >= 2 && batch <= 32 && nb >= 2 && nb % 2 == 0;
+}
 
 cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_rows, int k) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encoder();
@@ -527,7 +587,7 @@ cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_r
   const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k / kBlockWeights) * (kBlockBytes / 4),
                               static_cast<cuuint64_t>(n_rows)};
   const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(k / kBlockWeights) * kBlockBytes};
-  const cuuint32_t box[2] = {kBlockBytes / 4, kPairRows};
+  const cuuint32_t box[2] = {kBlockBytes / 4, kTileRows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(weights), gdim, gstride, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -536,7 +596,9 @@ cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_r
 }
 
 cudaError_t launch_tc(const LaunchArgs &a, const CUtensorMap &map) {
-  return a.batch <= 16 ? launch_tc_nm<16>(a, map) : launch_tc_nm<32>(a, map);
+  if (a.batch <= 8) return launch_tc_nm<8>(a, map);
+  if (a.batch <= 16) return launch_tc_nm<16>(a, map);
+  return launch_tc_nm<32>(a, map);
 }
 
 }  // namespace muse

@@ -44,7 +44,7 @@ cudaError_t launch_b1(const LaunchArgs &a);          // fused batch-1 kernel
 int generic_launches(const LaunchArgs &a);
 
 // Tensor-core path (batches 2..32): activation-package prep + tcgen05 kernel.
-bool tc_supported(int batch);
+bool tc_supported(int batch, int k);
 size_t tc_workspace_bytes(int k);
 cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_rows, int k);
 cudaError_t launch_tc(const LaunchArgs &a, const CUtensorMap &map);

@@ -58,7 +58,7 @@ enum class Path { B1, TensorCore, Generic };
 
 Path choose_path(const muse_lmhead *h, int batch) {
   if (batch == 1 && muse::b1_supported(static_cast<int>(h->k))) return Path::B1;
-  if (muse::tc_supported(batch)) return Path::TensorCore;
+  if (muse::tc_supported(batch, static_cast<int>(h->k))) return Path::TensorCore;
   return Path::Generic;
 }
 
