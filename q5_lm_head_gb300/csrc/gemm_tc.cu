@@ -50,7 +50,6 @@ namespace {
 
 constexpr int kTileRows = 128;                          // M of one MMA
 constexpr int kWStageBytes = kTileRows * kBlockBytes;   // 22,528: one block of a tile
-constexpr int kXStages = 2;
 constexpr int kUnpackWarps = 16;                        // 2 pairs x 2 warpgroups
 constexpr int kThreads = 32 * (kUnpackWarps + 3);       // + weight producer, MMA issuer, package producer
 constexpr int kProducerWarp = kUnpackWarps;
@@ -70,6 +69,9 @@ struct TcCfg {
   static constexpr int kXBytes = kXRows * kBlockWeights * 2;      // f16 [2NM][256] operand tile
   static constexpr int kMinBytes = min_rows<NM>() * 16 * 2;       // f16 [rows][16]
   static constexpr int kPkgBytes = kXBytes + kMinBytes;           // per block
+  // Package ring: a stage is refilled only after the MMAs that read it are
+  // complete, so the ring must cover the copy latency from L2 with a few steps.
+  static constexpr int kXStages = NM == 32 ? 3 : 4;
   static constexpr int kXchgBytes = 2 * kTileRows * (NM / 2) * 4; // pair-1 sums handed to pair 0
   static constexpr int kFixed = kXStages * kPkgBytes + kXchgBytes + 1024;
   static constexpr int kWFit = (kSmemLimit - kFixed) / kWStageBytes;
@@ -266,12 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int HB = NM / 2;                                      // batch columns per warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *wst = smem;                                            // [kWStages][128 rows][176 B]
-  uint8_t *xst = smem + C::kWStages * kWStageBytes;               // [kXStages][package]
-  float *xchg = reinterpret_cast<float *>(xst + kXStages * C::kPkgBytes);   // [2 halves][128][HB]
+  uint8_t *xst = smem + C::kWStages * kWStageBytes;               // [C::kXStages][package]
+  float *xchg = reinterpret_cast<float *>(xst + C::kXStages * C::kPkgBytes);   // [2 halves][128][HB]
   uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) + C::kXchgBytes);
   uint64_t *wfull = bars, *wempty = bars + C::kWStages;
-  uint64_t *xfull = wempty + C::kWStages, *xempty = xfull + kXStages;
-  uint64_t *aready = xempty + kXStages;                           // [2]: A written, D read
+  uint64_t *xfull = wempty + C::kWStages, *xempty = xfull + C::kXStages;
+  uint64_t *aready = xempty + C::kXStages;                           // [2]: A written, D read
   uint64_t *adone = aready + 2;                                   // [2]: MMAs of the buffer complete
   uint64_t *mma_idle = adone + 2;                                 // all MMAs of this CTA complete
   uint64_t *xch_full = mma_idle + 1, *xch_empty = mma_idle + 2;   // tile-end hand-over, pair 1 -> pair 0
@@ -289,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&wfull[s], 1);
       ptx::mbar_init(&wempty[s], 8);                              // the pair's eight warps
     }
-    for (int s = 0; s < kXStages; ++s) {
+    for (int s = 0; s < C::kXStages; ++s) {
       ptx::mbar_init(&xfull[s], 1);
       ptx::mbar_init(&xempty[s], 1);                              // one commit after the block's MMAs
     }
@@ -322,17 +324,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ weight producer
     if (lane == 0) {
       const uint64_t pol_w = ptx::policy_evict_first();
+      // step g = (tile, block kb) in tile-major order; counters instead of divisions
       int64_t issued = 0;
+      int kb = 0, ws = 0;
+      uint32_t ph = 0;                          // parity of the current pass over the ring
+      int64_t row0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
       for (int64_t g = 0; g < total && !*s_abort; ++g) {
-        const int64_t tile = blockIdx.x + (g / nb) * gridDim.x;
-        const int kb = static_cast<int>(g % nb);
-        const int ws = static_cast<int>(g % C::kWStages);
-        if (g >= C::kWStages &&
-            !ptx::mbar_wait(&wempty[ws], static_cast<uint32_t>((g / C::kWStages - 1) & 1))) { fail(); break; }
+        if (g >= C::kWStages && !ptx::mbar_wait(&wempty[ws], ph ^ 1u)) { fail(); break; }
         ptx::mbar_arrive_expect_tx(&wfull[ws], kWStageBytes);
-        tma_load_2d(wst + ws * kWStageBytes, &wmap, kb * (kBlockBytes / 4), static_cast<int>(tile * kTileRows),
-                    &wfull[ws], pol_w);
+        tma_load_2d(wst + ws * kWStageBytes, &wmap, kb * (kBlockBytes / 4), static_cast<int>(row0), &wfull[ws],
+                    pol_w);
         issued = g + 1;
+        if (++ws == C::kWStages) { ws = 0; ph ^= 1u; }
+        if (++kb == nb) { kb = 0; row0 += static_cast<int64_t>(gridDim.x) * kTileRows; }
       }
       // never leave copies in flight
       for (int64_t g = issued > C::kWStages ? issued - C::kWStages : 0; g < issued; ++g)
@@ -342,11 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ activation-package producer
     if (lane == 0) {
       int64_t issued = 0;
+      int kb = 0, xs = 0;
+      uint32_t ph = 0;
       for (int64_t g = 0; g < total && !*s_abort; ++g) {
-        const int kb = static_cast<int>(g % nb);
-        const int xs = static_cast<int>(g % kXStages);
-        if (g >= kXStages &&
-            !ptx::mbar_wait(&xempty[xs], static_cast<uint32_t>((g / kXStages - 1) & 1))) { fail(); break; }
+        if (g >= C::kXStages && !ptx::mbar_wait(&xempty[xs], ph ^ 1u)) { fail(); break; }
         ptx::mbar_arrive_expect_tx(&xfull[xs], C::kPkgBytes);
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                          ptx::smem_u32(xst + xs * C::kPkgBytes)),
@@ -354,20 +357,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                      "r"(ptx::smem_u32(&xfull[xs]))
                      : "memory");
         issued = g + 1;
+        if (++xs == C::kXStages) { xs = 0; ph ^= 1u; }
+        if (++kb == nb) kb = 0;
       }
-      for (int64_t g = issued > kXStages ? issued - kXStages : 0; g < issued; ++g)
-        ptx::mbar_wait(&xfull[g % kXStages], static_cast<uint32_t>((g / kXStages) & 1));
+      for (int64_t g = issued > C::kXStages ? issued - C::kXStages : 0; g < issued; ++g)
+        ptx::mbar_wait(&xfull[g % C::kXStages], static_cast<uint32_t>((g / C::kXStages) & 1));
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop (waits and operands stay warp-uniform); one
     // elected lane issues the MMAs and commits.
     bool ok = true;
+    int xs = 0;
+    uint32_t xph = 0;
     for (int64_t g = 0; g < total; ++g) {
       if (__any_sync(0xffffffffu, *s_abort != 0u)) break;
-      const int xs = static_cast<int>(g % kXStages);
       const int j = static_cast<int>(g & 1);
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&xfull[xs], static_cast<uint32_t>((g / kXStages) & 1)));
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(&xfull[xs], xph));
       if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&aready[j], static_cast<uint32_t>((g >> 1) & 1)));
       if (!ok) break;
       tc::fence_after();
@@ -385,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(&xempty[xs]);
       }
       __syncwarp();
+      if (++xs == C::kXStages) { xs = 0; xph ^= 1u; }
     }
     if (!ok && lane == 0) fail();
     // tensor memory is freed below only after every MMA issued here completed
@@ -461,12 +468,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       return ok;
     };
     bool ok_all = true;
-    int64_t tile_prev = -1;
-    for (int64_t g = p; g < total; g += 2) {
+    // The pair's steps g = p, p+2, ...: weight stage, ring parity, block and
+    // tile follow by counting (nb and the ring size are even).
+    int ws = p, kb = p;
+    uint32_t wph = 0;
+    int64_t tile = blockIdx.x, tile_prev = -1;
+    uint32_t i = 0;                             // the pair's step count
+    for (int64_t g = p; g < total; g += 2, ++i) {
       if (__any_sync(0xffffffffu, *s_abort != 0u)) { ok_all = false; break; }
-      const int64_t tile = blockIdx.x + (g / nb) * gridDim.x;
-      const int ws = static_cast<int>(g % C::kWStages);
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wfull[ws], static_cast<uint32_t>((g / C::kWStages) & 1)))) {
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wfull[ws], wph))) {
         if (lane == 0) fail();
         ok_all = false;
         break;
@@ -475,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       RowHdr hd;
       load_row_hdr(blk, hd);
       const uint32_t ta = tbase + lane_base + C::col_a(p) + 64 * hf;
-      if (g >= 2) {                             // buffer p: previous block's A consumed, D written
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&adone[p], static_cast<uint32_t>(((g - 2) >> 1) & 1)))) {
+      if (i > 0) {                              // buffer p: previous block's A consumed, D written
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&adone[p], (i - 1) & 1u))) {
           if (lane == 0) fail();
           ok_all = false;
           break;
@@ -504,13 +514,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       d_prev = hd.d;
       dmin_prev = hd.dmin;
       tile_prev = tile;
+      if ((ws += 2) >= C::kWStages) { ws -= C::kWStages; wph ^= 1u; }
+      if ((kb += 2) >= nb) { kb -= nb; tile += gridDim.x; }
     }
     // The pair's last block and the last tile.  Both pairs get here having
     // taken part in the same tile hand-overs: nb is even, so each pair owns
     // blocks of every tile.
-    if (ok_all && tile_prev >= 0) {
-      const int64_t g_last = p + ((total - 1 - p) / 2) * 2;
-      if (__all_sync(0xffffffffu, ptx::mbar_wait(&adone[p], static_cast<uint32_t>((g_last >> 1) & 1)))) {
+    if (ok_all && i > 0) {
+      if (__all_sync(0xffffffffu, ptx::mbar_wait(&adone[p], (i - 1) & 1u))) {
         drain();
         if (!finish_tile(tile_prev * kTileRows + r) && lane == 0) fail();
       } else if (lane == 0) {
