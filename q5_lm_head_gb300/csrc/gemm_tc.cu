@@ -3,16 +3,19 @@
 // cap, argmax ("Chapter 20 — Final norm, LM head, and the soft cap", §20.1,
 // §20.3, §20.4).  Two launches per forward:
 //
-// 1. prep_x_kernel: one CTA per Q5_K block column kb.  Normalises the hidden
-//    rows and writes, per block, an "activation package" already in the
-//    tensor-core operand layout (K-major, 8-row x 16-byte core matrices):
+// 1. prep_x_kernel: one CTA per (Q5_K block column kb, package row b).
+//    Normalises hidden row b and writes its part of the block's "activation
+//    package", already in the tensor-core operand layout (K-major, 8-row x
+//    16-byte core matrices):
 //      x     [2*NM rows][256]  rows 0..NM-1: f16(x); rows NM..2NM-1: f16(x - f16(x))
 //                              (the two rows of a batch row sum to x to ~2^-22)
 //      x_min [max(NM,16) rows][16]  k < 8: f16 hi of S_s = sum of x over
 //                              sub-block s, k >= 8: its f16 remainder
 //    Rows >= batch are zero.
 //
-// 2. gemm_tc_kernel: a persistent CTA per SM works on 128-row tiles.
+// 2. gemm_tc_kernel: a persistent CTA per SM works on 128-row tiles.  It is a
+//    programmatic dependent launch: everything but the package loads (set-up,
+//    the weight stream, the first unpack steps) overlaps the prep kernel.
 //    * weight producer warp: per block kb, one 2-D TMA box of 128 rows x 176
 //      bytes into a ring of weight stages.  Package producer warp: the kb
 //      activation package (1-D bulk copy) into a ring of package stages.
@@ -95,22 +98,30 @@ __host__ __device__ constexpr uint32_t kmajor_offset(int rows, int n, int k) {
 }
 
 // ------------------------------------------------------------------ prep kernel
+// Grid (nb, max(NM,16)), 128 threads; thread t covers columns t and t+128 of the
+// block, so warp w holds sub-blocks w and 4+w.
+constexpr int kPrepThreads = 128;
+
 template <int NM>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPrepThreads)
     prep_x_kernel(const float *__restrict__ hidden, const float *__restrict__ gamma, float eps, int batch, int k,
                   uint8_t *__restrict__ pkgs) {
   using C = TcCfg<NM>;
-  __shared__ float s_r[32];
-  __shared__ float s_part[8];
-  const int kb = blockIdx.x;
+  __shared__ float s_part[kPrepThreads / 32];
+  // let the dependent GEMM start its set-up and weight stream now; it reads the
+  // packages only after this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int kb = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // per-row RMS factors (every CTA recomputes them from the L2-resident rows)
-  for (int b = 0; b < batch; ++b) {
-    float r = 1.0f;
+  float x[2] = {0.0f, 0.0f};
+  if (b < batch) {
+    const float *h = hidden + static_cast<size_t>(b) * k;
+    const int c0 = kb * kBlockWeights + tid;
+    x[0] = h[c0];
+    x[1] = h[c0 + 128];
     if (gamma) {
       float ss = 0.0f;
-      const float *h = hidden + static_cast<size_t>(b) * k;
-      for (int j = tid * 4; j < k; j += 256 * 4) {
+      for (int j = tid * 4; j < k; j += kPrepThreads * 4) {
         const float4 v = *reinterpret_cast<const float4 *>(h + j);
         ss = fmaf(v.x, v.x, ss);
         ss = fmaf(v.y, v.y, ss);
@@ -121,34 +132,30 @@ __global__ void __launch_bounds__(256)
       if (lane == 0) s_part[warp] = ss;
       __syncthreads();
       float tot = 0.0f;
-      for (int i = 0; i < 8; ++i) tot += s_part[i];
-      r = 1.0f / sqrtf(tot / static_cast<float>(k) + eps);
-      __syncthreads();
+      for (int w = 0; w < kPrepThreads / 32; ++w) tot += s_part[w];
+      const float rr = 1.0f / sqrtf(tot / static_cast<float>(k) + eps);
+      x[0] *= rr * gamma[c0];
+      x[1] *= rr * gamma[c0 + 128];
     }
-    if (tid == 0) s_r[b] = r;
   }
-  __syncthreads();
   uint8_t *pkg = pkgs + static_cast<size_t>(kb) * C::kPkgBytes;
-  const int j = tid;                        // column inside the block; warp = sub-block
-  const int col = kb * kBlockWeights + j;
-  const float g = gamma ? gamma[col] : 1.0f;
-  for (int b = 0; b < min_rows<NM>(); ++b) {
-    float x = 0.0f;
-    if (b < batch) x = gamma ? hidden[static_cast<size_t>(b) * k + col] * s_r[b] * g
-                             : hidden[static_cast<size_t>(b) * k + col];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int j = tid + 128 * hh;           // column inside the block
     if (b < NM) {
-      const __half hi = __float2half_rn(x);
-      const __half lo = __float2half_rn(x - __half2float(hi));
+      const __half hi = __float2half_rn(x[hh]);
+      const __half lo = __float2half_rn(x[hh] - __half2float(hi));
       *reinterpret_cast<__half *>(pkg + kmajor_offset(C::kXRows, b, j)) = hi;
       *reinterpret_cast<__half *>(pkg + kmajor_offset(C::kXRows, NM + b, j)) = lo;
     }
-    float s = x;                            // sum over the 32 columns of sub-block `warp`
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    float sum = x[hh];                      // sum over the 32 columns of sub-block 4hh + warp
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) {
-      const __half shi = __float2half_rn(s);
-      const __half slo = __float2half_rn(s - __half2float(shi));
-      *reinterpret_cast<__half *>(pkg + C::kXBytes + kmajor_offset(min_rows<NM>(), b, warp)) = shi;
-      *reinterpret_cast<__half *>(pkg + C::kXBytes + kmajor_offset(min_rows<NM>(), b, 8 + warp)) = slo;
+      const int sb = 4 * hh + warp;
+      const __half shi = __float2half_rn(sum);
+      const __half slo = __float2half_rn(sum - __half2float(shi));
+      *reinterpret_cast<__half *>(pkg + C::kXBytes + kmajor_offset(min_rows<NM>(), b, sb)) = shi;
+      *reinterpret_cast<__half *>(pkg + C::kXBytes + kmajor_offset(min_rows<NM>(), b, 8 + sb)) = slo;
     }
   }
 }
@@ -345,6 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kPkgWarp) {
     // ------------------------------------------------------------ activation-package producer
     if (lane == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");   // the prep grid has completed
+
       int64_t issued = 0;
       int kb = 0, xs = 0;
       uint32_t ph = 0;
@@ -570,15 +579,25 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
     configured |= bit;
   }
   const int nb = a.k / kBlockWeights;
-  prep_x_kernel<NM><<<nb, 256, 0, a.stream>>>(a.hidden, a.gamma, a.eps, a.batch, a.k, a.ws.xpkg);
+  prep_x_kernel<NM><<<dim3(nb, min_rows<NM>()), kPrepThreads, 0, a.stream>>>(a.hidden, a.gamma, a.eps, a.batch,
+                                                                             a.k, a.ws.xpkg);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t n_tiles = (a.n_rows + kTileRows - 1) / kTileRows;
   const int64_t grid = n_tiles < a.num_sms ? n_tiles : a.num_sms;
-  gemm_tc_kernel<NM><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(
-      map, a.ws.xpkg, nb, a.n_rows, a.batch, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax,
-      a.ws.status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // may start before the prep grid ends
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NM>, map, static_cast<const uint8_t *>(a.ws.xpkg), nb,
+                            a.n_rows, a.batch, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax,
+                            a.ws.status);
 }
 
 }  // namespace
