@@ -10,16 +10,18 @@
 //     block add their row contributions with two shuffles and one of them
 //     writes the block's partial into a ring of partial slots.  Consumers wait
 //     for nothing but "stage full".
-//   * producer warp: moves tiles of kRows consecutive weight rows (contiguous
-//     in HBM) into a ring of shared-memory stages with 1-D bulk copies
-//     (cp.async.bulk + mbarrier transaction counts, L2 evict-first).  CTAs take
-//     tiles round-robin, so the whole GPU streams one contiguous stretch.  Each
-//     time consumers release a stage, the warp first re-arms it with the next
-//     tile and then finishes the released stage's rows: fixed-order sum of the
-//     block partials, scale + soft cap, store, argmax key.  The partial ring
-//     has one slot more than the stage ring, so a slot is never rewritten
-//     before the producer has read it (the rewrite needs a stage the producer
-//     arms only afterwards).
+//   * two producer warps: move tiles of kRows consecutive weight rows
+//     (contiguous in HBM) into a ring of shared-memory stages with 1-D bulk
+//     copies (cp.async.bulk + mbarrier transaction counts, L2 evict-first);
+//     producer p owns the stages of parity p, so two copies are always being
+//     armed independently.  CTAs take tiles round-robin, so the whole GPU
+//     streams one contiguous stretch.  Each time consumers release one of its
+//     stages, a producer first re-arms it with its next tile and then finishes
+//     the released stage's rows: fixed-order sum of the block partials, scale +
+//     soft cap, store, argmax key.  The partial ring has two slots more than
+//     the stage ring, so a slot is never rewritten before its producer has read
+//     it (the rewrite needs a stage that the same producer arms only
+//     afterwards).
 //
 // Arithmetic of a consumer thread (exact up to f32 rounding of the last steps)
 //   Its 64 normalised activations x_j are written as x_j = sigma * xi_j with a
@@ -40,7 +42,7 @@
 namespace muse {
 namespace {
 
-constexpr int kRows = 8;            // weight rows per pipeline stage
+constexpr int kRows = 12;           // weight rows per pipeline stage (one 1-D bulk copy)
 constexpr int kStreams = 4;         // row teams of consumer threads
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // opt-in limit minus static shared memory
 constexpr float kQuantMax = 8388600.0f;   // |xi| stays below 2^23 after rounding
@@ -51,17 +53,18 @@ struct B1Cfg {
   static constexpr int kConsumers = kUnits * kStreams;
   static_assert(kConsumers % 32 == 0, "consumer threads must fill whole warps");
   static_assert(kUnits % 4 == 0, "the four units of a block stay inside one stream");
+  static_assert(kRows % kStreams == 0, "each stream takes the same number of rows");
   static constexpr int kConsumerWarps = kConsumers / 32;
-  static constexpr int kProducerWarp = kConsumerWarps;
-  static constexpr int kThreads = kConsumers + 32;
+  static constexpr int kProducerWarps = 2;
+  static constexpr int kThreads = kConsumers + 32 * kProducerWarps;
   static constexpr int kRowBytes = NB * kBlockBytes;
   static constexpr int kStageBytes = kRows * kRowBytes;
   static constexpr int kSlotBytes = kRows * NB * 4;         // one partial per (row, block)
   static constexpr int kFixedBytes = 512;                   // barriers + scratch
-  static constexpr int kStagesFit = (kMaxSmem - kFixedBytes - kSlotBytes) / (kStageBytes + kSlotBytes);
-  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  static_assert(kStages >= 2, "need at least double buffering");
-  static constexpr int kSlots = kStages + 1;
+  static constexpr int kStagesFit = (kMaxSmem - kFixedBytes - 2 * kSlotBytes) / (kStageBytes + kSlotBytes);
+  static constexpr int kStages = (kStagesFit > 8 ? 8 : kStagesFit) & ~1;   // even: one parity per producer
+  static_assert(kStages >= 4, "need at least double buffering per producer");
+  static constexpr int kSlots = kStages + 2;
   static constexpr int kSmemBytes = kStages * kStageBytes + kSlots * kSlotBytes + kFixedBytes;
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
 };
@@ -189,22 +192,28 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
     *s_abort = 1u;
   };
 
-  if (warp == C::kProducerWarp) {
-    // ------------------------------------------------------------ producer + row epilogue
+  if (warp >= C::kConsumerWarps) {
+    // ------------------------------------------------------------ producers + row epilogue
+    // Producer pw handles the CTA's tiles of local index j = pw, pw+2, ...: stage
+    // j % kStages and partial slot j % kSlots (both rings have even length).
+    const int pw = warp - C::kConsumerWarps;
     const uint64_t policy = ptx::policy_evict_first();
-    const int er = lane >> 2, eq = lane & 3;   // epilogue: row er, every 4th block partial from eq
+    // epilogue: lane pair (2er, 2er+1) sums row er's block partials, alternating
+    static_assert(kRows <= 16, "two lanes per row");
+    const int er = lane >> 1, eq = lane & 1;
     unsigned long long best = 0ull;
-    // finish the rows of stage j (its consumers have released it)
+    // finish the rows of local tile j (its consumers have released its stage)
     auto finish = [&](int j) {
       const int64_t r0 = (blockIdx.x + static_cast<int64_t>(j) * gridDim.x) * kRows;
       const float *pr = slots + (j % C::kSlots) * (C::kSlotBytes / 4) + er * NB;
       float sacc = 0.0f;
+      if (er < kRows) {
 #pragma unroll
-      for (int g = 0; g < NB; g += 4)
-        if (g + eq < NB) sacc += pr[g + eq];
+        for (int g = 0; g < NB; g += 2)
+          if (g + eq < NB) sacc += pr[g + eq];
+      }
       sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
-      sacc += __shfl_xor_sync(0xffffffffu, sacc, 2);
-      if (eq == 0 && r0 + er < n_rows) {
+      if (eq == 0 && er < kRows && r0 + er < n_rows) {
         const int64_t row = r0 + er;
         const float out = scale_softcap(sacc, scale, cap);
         logits[row] = out;
@@ -217,28 +226,31 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
       if (lane == 0) ok = ptx::mbar_wait(&empty[j % C::kStages], static_cast<uint32_t>((j / C::kStages) & 1));
       return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     };
-    int issued = 0, st = 0;
+    const int my_tiles = blockIdx.x < n_tiles ? static_cast<int>((n_tiles - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
+    int issued = pw;                           // next local tile of this producer
     bool aborted = false;
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    for (; issued < my_tiles; issued += 2) {
       if (__any_sync(0xffffffffu, *s_abort != 0u)) { aborted = true; break; }
-      if (issued >= C::kStages && !wait_released(issued - C::kStages)) {
+      const int j = issued;
+      if (j >= C::kStages && !wait_released(j - C::kStages)) {
         if (lane == 0) fail();
         aborted = true;
         break;
       }
       if (lane == 0) {
-        const int64_t r0 = tile * kRows;
+        const int64_t r0 = (blockIdx.x + static_cast<int64_t>(j) * gridDim.x) * kRows;
         const int rows = n_rows - r0 < kRows ? static_cast<int>(n_rows - r0) : kRows;
         const uint32_t bytes = static_cast<uint32_t>(rows * C::kRowBytes);
+        const int st = j % C::kStages;
         ptx::mbar_arrive_expect_tx(&full[st], bytes);
         ptx::bulk_g2s(stages + st * C::kStageBytes, w + r0 * C::kRowBytes, bytes, &full[st], policy);
       }
-      if (issued >= C::kStages) finish(issued - C::kStages);
-      ++issued;
-      if (++st == C::kStages) st = 0;
+      if (j >= C::kStages) finish(j - C::kStages);
     }
-    const int first = issued > C::kStages ? issued - C::kStages : 0;
-    for (int j = first; j < issued && !aborted; ++j) {
+    // the last tiles this producer armed: wait for their release, finish them
+    int first = issued - C::kStages;
+    if (first < pw) first = pw;
+    for (int j = first; j < issued && !aborted; j += 2) {
       if (__any_sync(0xffffffffu, *s_abort != 0u) || !wait_released(j)) {
         if (lane == 0) fail();
         aborted = true;
@@ -248,11 +260,11 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
     }
     if (aborted && lane == 0) {
       // never leave the CTA with copies in flight: wait (bounded) for the fills armed last
-      for (int j = first; j < issued; ++j)
+      for (int j = first; j < issued; j += 2)
         ptx::mbar_wait(&full[j % C::kStages], static_cast<uint32_t>((j / C::kStages) & 1));
     }
     for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
-    if (lane == 0) *s_best = best;
+    if (lane == 0 && best != 0ull) atomicMax(s_best, best);
   } else {
     // ------------------------------------------------------------ consumers
     const int stream = tid / C::kUnits;
