@@ -227,6 +227,38 @@ def _e2e(args, wl, head, hidden, w_d, g_d, eps, stream, ws, nbytes):
             "d2h_bytes_per_step": d2h, "us_per_forward": round(secs * 1e6, 2)}
 
 
+def _hold_cycles(steps: int) -> int:
+    """GPU cycles to sleep while the host enqueues `steps` timed forwards
+    (about 0.3 ms of host work per step, at up to 2.1 GHz)."""
+    return int(min(2.0, 0.3e-3 * (steps + 4)) * 2.1e9)
+
+
+def _graph_times(fwd, stream, steps, l2_flush):
+    """Median device time of one forward replayed from a captured CUDA graph,
+    L2 flushed before each replay; None when capture fails."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fwd()
+        torch.cuda.synchronize()
+    except RuntimeError as e:   # capture unsupported: report, do not fail the bench
+        return {"error": str(e).splitlines()[0][:200]}
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        g.replay()
+        torch.cuda._sleep(_hold_cycles(steps))
+        for i in range(steps):
+            l2_flush(i)
+            starts[i].record(stream)
+            g.replay()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    per = [s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends)]
+    return {"us_per_forward_median": round(statistics.median(per), 2), "steps": steps}
+
+
 def run_ours(args, wl):
     import numpy as np
     import torch
@@ -257,8 +289,14 @@ def run_ours(args, wl):
     eps = synth.RMS_EPS
     big = wl.algorithmic_bytes() > 2 * L2_BYTES
     l2_mode = ("inputs larger than L2 (weights stream from HBM every forward)" if big else
-               "L2 flushed before every timed forward (256 MiB write, outside the timed interval)")
+               "L2 flushed before every timed forward (256 MiB write, then a 256 MiB read so that no "
+               "write-back lands in the timed interval; both outside it)")
     flush = None if big else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    evict = None if big else torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+
+    def l2_flush(i):
+        flush.fill_(i & 0xFF)
+        evict.sum()
 
     def fwd():
         head.forward(h_d, w_d, g_d, eps, wl.scale, wl.cap, wl.argmax, logits, amax, stream)
@@ -279,10 +317,13 @@ def run_ours(args, wl):
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        # hold the GPU while the host enqueues every timed step, so that no
+        # interval below waits on the host
+        torch.cuda._sleep(_hold_cycles(args.steps))
         t_begin.record(stream)
         for i in range(args.steps):
             if flush is not None:
-                flush.fill_(i & 0xFF)
+                l2_flush(i)
             starts[i].record(stream)
             fwd()
             ends[i].record(stream)
@@ -294,7 +335,12 @@ def run_ours(args, wl):
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]     # ms, each forward
     kern_ms = sum(per) / len(per)
     wall_ms = t_begin.elapsed_time(t_end)
-    step_ms = kern_ms if flush is not None else wall_ms / args.steps
+    step_ms = statistics.median(per) if flush is not None else wall_ms / args.steps
+
+    # small workloads: the same forward replayed from a CUDA graph (launch cost off the host path)
+    graph = None
+    if flush is not None and not args.no_graph:
+        graph = _graph_times(fwd, stream, args.steps, l2_flush)
     if ws > 1:
         t = torch.tensor([step_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -317,6 +363,9 @@ def run_ours(args, wl):
         "data": "synthetic (seeded Q5_K weights and N(0,1) hidden rows; no checkpoint)",
         "config": _config(wl, ws, l2_mode),
         "us_per_forward": round(step_ms * 1e3, 2),
+        "us_per_forward_stat": "median of per-forward CUDA-event intervals" if flush is not None
+                               else "timed wall interval / steps",
+        "cuda_graph": graph,
         "logits_per_s": round(ws * wl.batch * wl.n_rows / (step_ms * 1e-3), 1),
         "pct_of_peak": round(100.0 * achieved / peak, 2),
         "kernel_path": head.path_name(wl.batch),
@@ -351,6 +400,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="lmhead_b1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

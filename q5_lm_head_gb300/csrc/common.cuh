@@ -82,4 +82,34 @@ __device__ __forceinline__ void argmax_finish(unsigned long long *keys, unsigned
   }
 }
 
+// Same result as argmax_finish, for a CTA whose per-batch-row keys sit in
+// shared memory (cta_keys[b], 0 = none; final when the CTA calls this): one
+// thread adds them with fire-and-forget max reductions and takes a ticket with
+// acquire-release semantics (the release orders its reductions before the
+// ticket), so the CTA pays a single global round trip; the last CTA reads the
+// keys (acquire through the ticket) and re-arms keys and ticket.
+__device__ __forceinline__ void argmax_publish_finish(unsigned long long *keys, unsigned int *ticket,
+                                                      int32_t *argmax, const unsigned long long *cta_keys,
+                                                      int batch) {
+  __shared__ unsigned int s_last;
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < batch; ++b)
+      if (cta_keys[b] != 0ull)
+        asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(keys + b), "l"(cta_keys[b]) : "memory");
+    unsigned int t;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(ticket) : "memory");
+    s_last = (t == gridDim.x - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (s_last) {
+    for (int b = threadIdx.x; b < batch; b += blockDim.x) {
+      unsigned long long key;
+      asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(key) : "l"(keys + b) : "memory");
+      argmax[b] = (int32_t)argmax_key_index(key);
+      asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(keys + b), "l"(0ull) : "memory");
+    }
+    if (threadIdx.x == 0) asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(ticket), "r"(0u) : "memory");
+  }
+}
+
 }  // namespace muse

@@ -22,6 +22,12 @@
 //     the stage ring, so a slot is never rewritten before its producer has read
 //     it (the rewrite needs a stage that the same producer arms only
 //     afterwards).
+//   * prologue: the producer that owns the last stage first fills it with the
+//     hidden row (and gamma) in one bulk copy per tensor; the consumers build
+//     the RMS factor and their activations from shared memory, then release
+//     the stage, and only then is it armed with its first weight tile.  Every
+//     CTA needs the whole row, so one copy per CTA replaces 4x redundant
+//     per-thread loads of the same bytes by all CTAs at once.
 //
 // Arithmetic of a consumer thread (exact up to f32 rounding of the last steps)
 //   Its 64 normalised activations x_j are written as x_j = sigma * xi_j with a
@@ -67,6 +73,7 @@ struct B1Cfg {
   static constexpr int kSlots = kStages + 2;
   static constexpr int kSmemBytes = kStages * kStageBytes + kSlots * kSlotBytes + kFixedBytes;
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
+  static_assert(2 * NB * kBlockWeights * 4 <= kStageBytes, "hidden + gamma fit one stage");
 };
 
 __device__ __forceinline__ uint32_t rotl32(uint32_t v, uint32_t s) { return __funnelshift_l(v, v, s); }
@@ -168,7 +175,12 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
   float *slots = reinterpret_cast<float *>(smem + C::kStages * C::kStageBytes);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes + C::kSlots * C::kSlotBytes);
   uint64_t *empty = full + C::kStages;
-  float *s_red = reinterpret_cast<float *>(empty + C::kStages);            // [32]
+  uint64_t *pro_full = empty + C::kStages;                                 // hidden (+ gamma) staged
+  uint64_t *pro_done = pro_full + 1;                                       // consumers done with them
+  float *s_red = reinterpret_cast<float *>(pro_done + 1);                  // [32]
+  // the prologue's staging area: the last stage, until its first weight tile
+  const float *s_hidden = reinterpret_cast<const float *>(stages + (C::kStages - 1) * C::kStageBytes);
+  const float *s_gamma = s_hidden + K;
   unsigned long long *s_best = reinterpret_cast<unsigned long long *>(s_red + 32);
   volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(s_best + 1);
 
@@ -181,6 +193,8 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], C::kConsumerWarps);
     }
+    ptx::mbar_init(pro_full, 1);
+    ptx::mbar_init(pro_done, C::kConsumerWarps);
     *s_best = 0ull;
     *s_abort = 0u;
     ptx::fence_barrier_init();
@@ -198,6 +212,14 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
     // j % kStages and partial slot j % kSlots (both rings have even length).
     const int pw = warp - C::kConsumerWarps;
     const uint64_t policy = ptx::policy_evict_first();
+    constexpr int kHoldTile = C::kStages - 1;  // local tile whose stage holds the prologue data
+    if (pw == (kHoldTile & 1) && lane == 0) {
+      const uint32_t row_bytes = static_cast<uint32_t>(K) * 4u;
+      uint8_t *dst = stages + kHoldTile * C::kStageBytes;
+      ptx::mbar_arrive_expect_tx(pro_full, gamma ? 2u * row_bytes : row_bytes);
+      ptx::bulk_g2s_nohint(dst, hidden, row_bytes, pro_full);
+      if (gamma) ptx::bulk_g2s_nohint(dst + row_bytes, gamma, row_bytes, pro_full);
+    }
     // epilogue: lane pair (2er, 2er+1) sums row er's block partials, alternating
     static_assert(kRows <= 16, "two lanes per row");
     const int er = lane >> 1, eq = lane & 1;
@@ -237,6 +259,15 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
         aborted = true;
         break;
       }
+      if (j == kHoldTile) {                    // the consumers still read the prologue data there
+        bool ok = true;
+        if (lane == 0) ok = ptx::mbar_wait(pro_done, 0);
+        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) {
+          if (lane == 0) fail();
+          aborted = true;
+          break;
+        }
+      }
       if (lane == 0) {
         const int64_t r0 = (blockIdx.x + static_cast<int64_t>(j) * gridDim.x) * kRows;
         const int rows = n_rows - r0 < kRows ? static_cast<int>(n_rows - r0) : kRows;
@@ -271,12 +302,15 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
     const int u = tid % C::kUnits;
     const int kb = u >> 2, c = u & 3;
 
-    // Final RMSNorm prologue (every CTA recomputes r from the L2-resident hidden row).
+    // Prologue: the hidden row (and gamma) arrive in the last stage.
+    bool pro_ok = __all_sync(0xffffffffu, ptx::mbar_wait(pro_full, 0));
+    if (!pro_ok && lane == 0) fail();
+    // Final RMSNorm: every CTA recomputes r from the staged row.
     float r = 1.0f;
     if (gamma) {
       float ss = 0.0f;
       for (int j = tid * 4; j < K; j += C::kConsumers * 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(hidden + j);
+        const float4 v = *reinterpret_cast<const float4 *>(s_hidden + j);
         ss = fmaf(v.x, v.x, ss);
         ss = fmaf(v.y, v.y, ss);
         ss = fmaf(v.z, v.z, ss);
@@ -297,11 +331,11 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
       const int col = kb * kBlockWeights + 64 * c;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        float4 hl = *reinterpret_cast<const float4 *>(hidden + col + 4 * i);
-        float4 hh = *reinterpret_cast<const float4 *>(hidden + col + 32 + 4 * i);
+        float4 hl = *reinterpret_cast<const float4 *>(s_hidden + col + 4 * i);
+        float4 hh = *reinterpret_cast<const float4 *>(s_hidden + col + 32 + 4 * i);
         if (gamma) {
-          const float4 gl = *reinterpret_cast<const float4 *>(gamma + col + 4 * i);
-          const float4 gh = *reinterpret_cast<const float4 *>(gamma + col + 32 + 4 * i);
+          const float4 gl = *reinterpret_cast<const float4 *>(s_gamma + col + 4 * i);
+          const float4 gh = *reinterpret_cast<const float4 *>(s_gamma + col + 32 + 4 * i);
           hl = make_float4(hl.x * r * gl.x, hl.y * r * gl.y, hl.z * r * gl.z, hl.w * r * gl.w);
           hh = make_float4(hh.x * r * gh.x, hh.y * r * gh.y, hh.z * r * gh.z, hh.w * r * gh.w);
         }
@@ -315,6 +349,9 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
         sx_hi += x_hi[l];
         amax = fmaxf(amax, fmaxf(fabsf(x_lo[l]), fabsf(x_hi[l])));
       }
+      // every staged value has been consumed: this warp no longer reads the staging area
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(pro_done);
       const float inv = amax > 0.0f ? kQuantMax / amax : 0.0f;
       sigma_half = amax > 0.0f ? 0.5f / inv : 0.0f;   // the 1/2 undoes the 2q form of the high nibbles
       quantize_planes(x_lo, inv, xl);
@@ -324,7 +361,7 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
 
     int st = 0, ps = 0;
     uint32_t ph = 0;                           // round parity of the stage ring
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    for (int64_t tile = blockIdx.x; tile < n_tiles && pro_ok; tile += gridDim.x) {
       // every exit decision is taken by the whole warp (the loop body shuffles)
       if (__any_sync(0xffffffffu, *s_abort != 0u)) break;
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full[st], ph))) {
@@ -364,10 +401,7 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
   }
 
   __syncthreads();
-  if (argmax) {
-    if (tid == 0 && *s_best != 0ull) atomicMax(keys, *s_best);
-    argmax_finish(keys, ticket, argmax, 1);
-  }
+  if (argmax) argmax_publish_finish(keys, ticket, argmax, s_best, 1);
 }
 
 template <int NB>
