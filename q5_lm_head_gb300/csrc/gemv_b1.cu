@@ -83,20 +83,30 @@ struct XPlanes {
   uint32_t p2[8], p1[8], p0[8];   // word i holds positions 4i..4i+3
 };
 
-__device__ __forceinline__ void quantize_planes(const float (&x)[32], float inv, XPlanes &out) {
+// Bytes t of the three planes of four consecutive activations.
+__device__ __forceinline__ void quantize_chunk(const float (&x)[4], float inv, uint32_t &w2, uint32_t &w1,
+                                               uint32_t &w0) {
+  w2 = w1 = w0 = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t w2 = 0, w1 = 0, w0 = 0;
+  for (int t = 0; t < 4; ++t) {
+    const int xi = __float2int_rn(x[t] * inv);
+    w2 |= (static_cast<uint32_t>(xi >> 16) & 0xFFu) << (8 * t);
+    w1 |= (static_cast<uint32_t>(xi >> 8) & 0xFFu) << (8 * t);
+    w0 |= (static_cast<uint32_t>(xi) & 0xFFu) << (8 * t);
+  }
+}
+
+// w[k] <- w[(k - rot) mod 16] for rot in 0..7 (three conditional rotation stages).
+__device__ __forceinline__ void rotate16_right(uint32_t (&w)[16], int rot) {
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int xi = __float2int_rn(x[4 * i + t] * inv);
-      w2 |= (static_cast<uint32_t>(xi >> 16) & 0xFFu) << (8 * t);
-      w1 |= (static_cast<uint32_t>(xi >> 8) & 0xFFu) << (8 * t);
-      w0 |= (static_cast<uint32_t>(xi) & 0xFFu) << (8 * t);
+  for (int b = 1; b <= 4; b <<= 1) {
+    if (rot & b) {
+      uint32_t t[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) t[k] = w[(k - b) & 15];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) w[k] = t[k];
     }
-    out.p2[i] = w2;
-    out.p1[i] = w1;
-    out.p0[i] = w0;
   }
 }
 
@@ -323,39 +333,53 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
       for (int i = 0; i < C::kConsumerWarps; ++i) tot += s_red[i];
       r = 1.0f / sqrtf(tot / static_cast<float>(K) + eps);
     }
-    // This thread's 64 activations, x_lo for sub-block 2c and x_hi for 2c+1.
+    // This thread's 64 activations: sub-block 2c (x_lo, chunks 0..7 of four) and
+    // 2c+1 (x_hi, chunks 8..15).  Thread u's 64 columns start 256 B after
+    // thread u-1's, so in natural order every lane of a warp would read the same
+    // shared-memory banks; lane l reads its chunks in the order (i + l) mod 16,
+    // l taken mod 8 (the eight lanes of each quarter-warp then cover all banks),
+    // does all elementwise work in that order and rotates the finished plane
+    // words back.
     XPlanes xl, xh;
     float sx_lo = 0.0f, sx_hi = 0.0f, sigma_half;
     {
-      float x_lo[32], x_hi[32];
+      const int rot = lane & 7;
       const int col = kb * kBlockWeights + 64 * c;
+      float xv[16][4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float4 hl = *reinterpret_cast<const float4 *>(s_hidden + col + 4 * i);
-        float4 hh = *reinterpret_cast<const float4 *>(s_hidden + col + 32 + 4 * i);
+      for (int i = 0; i < 16; ++i) {
+        const int gch = (i + rot) & 15;                   // chunk in natural order
+        const int off = col + 32 * (gch >> 3) + 4 * (gch & 7);
+        float4 h = *reinterpret_cast<const float4 *>(s_hidden + off);
         if (gamma) {
-          const float4 gl = *reinterpret_cast<const float4 *>(s_gamma + col + 4 * i);
-          const float4 gh = *reinterpret_cast<const float4 *>(s_gamma + col + 32 + 4 * i);
-          hl = make_float4(hl.x * r * gl.x, hl.y * r * gl.y, hl.z * r * gl.z, hl.w * r * gl.w);
-          hh = make_float4(hh.x * r * gh.x, hh.y * r * gh.y, hh.z * r * gh.z, hh.w * r * gh.w);
+          const float4 g = *reinterpret_cast<const float4 *>(s_gamma + off);
+          h = make_float4(h.x * r * g.x, h.y * r * g.y, h.z * r * g.z, h.w * r * g.w);
         }
-        x_lo[4 * i + 0] = hl.x; x_lo[4 * i + 1] = hl.y; x_lo[4 * i + 2] = hl.z; x_lo[4 * i + 3] = hl.w;
-        x_hi[4 * i + 0] = hh.x; x_hi[4 * i + 1] = hh.y; x_hi[4 * i + 2] = hh.z; x_hi[4 * i + 3] = hh.w;
+        xv[i][0] = h.x; xv[i][1] = h.y; xv[i][2] = h.z; xv[i][3] = h.w;
       }
       float amax = 0.0f;
 #pragma unroll
-      for (int l = 0; l < 32; ++l) {
-        sx_lo += x_lo[l];
-        sx_hi += x_hi[l];
-        amax = fmaxf(amax, fmaxf(fabsf(x_lo[l]), fabsf(x_hi[l])));
+      for (int i = 0; i < 16; ++i) {
+        const float cs = (xv[i][0] + xv[i][1]) + (xv[i][2] + xv[i][3]);
+        if (((i + rot) & 15) < 8) sx_lo += cs; else sx_hi += cs;
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(xv[i][0]), fabsf(xv[i][1])), fmaxf(fabsf(xv[i][2]), fabsf(xv[i][3]))));
       }
       // every staged value has been consumed: this warp no longer reads the staging area
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(pro_done);
       const float inv = amax > 0.0f ? kQuantMax / amax : 0.0f;
       sigma_half = amax > 0.0f ? 0.5f / inv : 0.0f;   // the 1/2 undoes the 2q form of the high nibbles
-      quantize_planes(x_lo, inv, xl);
-      quantize_planes(x_hi, inv, xh);
+      uint32_t w2[16], w1[16], w0[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) quantize_chunk(xv[i], inv, w2[i], w1[i], w0[i]);
+      rotate16_right(w2, rot);
+      rotate16_right(w1, rot);
+      rotate16_right(w0, rot);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        xl.p2[i] = w2[i]; xl.p1[i] = w1[i]; xl.p0[i] = w0[i];
+        xh.p2[i] = w2[8 + i]; xh.p1[i] = w1[8 + i]; xh.p0[i] = w0[8 + i];
+      }
     }
     const UnitSel us = make_unit_sel(c);
 
