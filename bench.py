@@ -142,7 +142,7 @@ def _dist():
 def _oracle_rate(wl, hidden, gamma, wq, target_s: float):
     """Time the oracle, as it stands, on a bounded sample of the workload: the
     first `rows` weight rows (all of them when they fit the time budget), run
-    `reps` times.  Returns (bytes_per_s, rows, reps, cores, secs)."""
+    repeatedly for `target_s` seconds.  Returns (bytes_per_s, rows, reps, cores, secs)."""
     import numpy as np
     import oracle
     cores = oracle.default_threads()
@@ -151,12 +151,15 @@ def _oracle_rate(wl, hidden, gamma, wq, target_s: float):
     oracle.lmhead(hidden, gamma, wq[:probe], wl.scale, wl.cap, nthreads=cores)
     dt = max(time.perf_counter() - t0, 1e-6)
     rows = int(min(wl.n_rows, max(probe, probe * target_s / dt)))
-    reps = max(1, int(target_s / (dt * rows / probe)))
     sample = np.ascontiguousarray(wq[:rows])
+    reps = 0
     t0 = time.perf_counter()
-    for _ in range(reps):
+    while True:                  # whole passes until the time budget is spent
         oracle.lmhead(hidden, gamma, sample, wl.scale, wl.cap, nthreads=cores)
-    secs = time.perf_counter() - t0
+        reps += 1
+        secs = time.perf_counter() - t0
+        if secs >= target_s:
+            break
     bytes_sample = wl.algorithmic_bytes() * (rows / wl.n_rows) * reps
     return bytes_sample / secs, rows, reps, cores, secs
 
@@ -402,7 +405,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="lmhead_b1", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
-    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--rows", type=int, default=0,
