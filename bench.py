@@ -139,6 +139,20 @@ def _dist():
     return ws, rank, local
 
 
+def replica_aggregate(seconds: float, nbytes: int, device=None):
+    """Whole-job throughput of independent replicas, one per rank: the bytes of
+    every rank over the slowest rank's time (max over ranks; the identity at one
+    rank).  Returns (GB/s, max seconds)."""
+    import torch
+    dist = torch.distributed
+    ws = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    if ws > 1:
+        t = torch.tensor([seconds], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        seconds = float(t.item())
+    return ws * nbytes / seconds / 1e9, seconds
+
+
 def _oracle_rate(wl, hidden, gamma, wq, target_s: float):
     """Time the oracle, as it stands, on a bounded sample of the workload: the
     first `rows` weight rows (all of them when they fit the time budget), run
@@ -221,13 +235,10 @@ def _e2e(args, wl, head, hidden, w_d, g_d, eps, stream, ws, nbytes):
     for _ in range(steps):
         head.forward_host(h_pin, w_d, g_d, eps, wl.scale, wl.cap, l_pin, a_pin, stream)
     secs = (time.perf_counter() - t0) / steps
-    if ws > 1:
-        t = torch.tensor([secs], device=w_d.device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        secs = float(t.item())
+    value, secs = replica_aggregate(secs, nbytes, w_d.device)
     h2d = wl.batch * wl.k * 4
     d2h = wl.batch * wl.n_rows * 4 + wl.batch * 4
-    return {"value": round(ws * nbytes / secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "us_per_forward": round(secs * 1e6, 2)}
 
 
@@ -345,12 +356,9 @@ def run_ours(args, wl):
     graph = None
     if flush is not None and not args.no_graph:
         graph = _graph_times(fwd, stream, args.steps, l2_flush)
-    if ws > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
     nbytes = wl.algorithmic_bytes()
-    value = ws * nbytes / (step_ms * 1e-3) / 1e9
+    value, step_s = replica_aggregate(step_ms * 1e-3, nbytes, dev)
+    step_ms = step_s * 1e3
     status = head.device_status()
 
     # end to end through the host-buffer entry point: pinned hidden in, logits + argmax out
