@@ -23,16 +23,16 @@
 //     it (the rewrite needs a stage that the same producer arms only
 //     afterwards).
 //   * prologue: the producer that owns the last stage first fills it with the
-//     hidden row (and gamma) in one bulk copy per tensor; the consumers build
-//     the RMS factor and their activations from shared memory, then release
-//     the stage, and only then is it armed with its first weight tile.  Every
-//     CTA needs the whole row, so one copy per CTA replaces 4x redundant
-//     per-thread loads of the same bytes by all CTAs at once.
+//     hidden row (and gamma), one bulk copy per tensor;
+//     the consumers build the RMS factor and their activation planes from
+//     shared memory (the four threads of a unit each quantise a quarter of its
+//     64 columns and share the plane words through the same stage), then
+//     release the stage, and only then is it armed with its first weight tile.
 //
 // Arithmetic of a consumer thread (exact up to f32 rounding of the last steps)
 //   Its 64 normalised activations x_j are written as x_j = sigma * xi_j with a
-//   per-thread sigma = max|x| / 8388600 and 24-bit integers xi_j, stored as three
-//   byte planes xi = 65536*x2 + 256*x1 + x0 (x2 signed, x1 and x0 unsigned).
+//   per-thread sigma = max|x| / 4194300 and integers |xi_j| < 2^22, stored as
+//   three byte planes xi = 65536*x2 + 256*x1 + x0 (x2 signed, x1 and x0 unsigned).
 //   For each sub-block s, sum_j q_j xi_j is built with dp4a on four 5-bit quants
 //   per word (low nibble | high bit << 4; high nibbles are taken as 2q so no
 //   extra shift is needed) against each plane, in exact integer arithmetic.
@@ -51,7 +51,8 @@ namespace {
 constexpr int kRows = 12;           // weight rows per pipeline stage (one 1-D bulk copy)
 constexpr int kStreams = 4;         // row teams of consumer threads
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // opt-in limit minus static shared memory
-constexpr float kQuantMax = 8388600.0f;   // |xi| stays below 2^23 after rounding
+constexpr float kQuantMax = 4194300.0f;   // |xi| stays below 2^22 after rounding
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 
 template <int NB>
 struct B1Cfg {
@@ -74,6 +75,14 @@ struct B1Cfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + kSlots * kSlotBytes + kFixedBytes;
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
   static_assert(2 * NB * kBlockWeights * 4 <= kStageBytes, "hidden + gamma fit one stage");
+  // after the activations are loaded the staging stage holds, per unit, the
+  // four (amax, sum) pairs of its quarters and its plane words (p2, p1, p0:
+  // 16 words each, padded to 52 so the units' rows fall on distinct banks)
+  static constexpr int kPlaneStride = 52;
+  static constexpr int kExBytes = kUnits * 4 * 8;
+  static constexpr int kPlaneOffset = 4096;
+  static_assert(kExBytes <= kPlaneOffset, "exchange area");
+  static_assert(kPlaneOffset + kUnits * kPlaneStride * 4 <= kStageBytes, "plane area");
 };
 
 __device__ __forceinline__ uint32_t rotl32(uint32_t v, uint32_t s) { return __funnelshift_l(v, v, s); }
@@ -83,31 +92,24 @@ struct XPlanes {
   uint32_t p2[8], p1[8], p0[8];   // word i holds positions 4i..4i+3
 };
 
-// Bytes t of the three planes of four consecutive activations.
+// The three plane words (byte t = activation t) of four consecutive activations.
+// fmaf(x, inv, 1.5*2^23) rounds x*inv to the nearest integer (ties to even) in
+// the mantissa: for |xi| < 2^22 its bits are 0x4B400000 + xi, so bytes 0 and 1
+// are those of xi and byte 2 is xi's signed high byte plus 0x40.
 __device__ __forceinline__ void quantize_chunk(const float (&x)[4], float inv, uint32_t &w2, uint32_t &w1,
                                                uint32_t &w0) {
-  w2 = w1 = w0 = 0;
+  uint32_t b[4];
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int xi = __float2int_rn(x[t] * inv);
-    w2 |= (static_cast<uint32_t>(xi >> 16) & 0xFFu) << (8 * t);
-    w1 |= (static_cast<uint32_t>(xi >> 8) & 0xFFu) << (8 * t);
-    w0 |= (static_cast<uint32_t>(xi) & 0xFFu) << (8 * t);
-  }
-}
-
-// w[k] <- w[(k - rot) mod 16] for rot in 0..7 (three conditional rotation stages).
-__device__ __forceinline__ void rotate16_right(uint32_t (&w)[16], int rot) {
-#pragma unroll
-  for (int b = 1; b <= 4; b <<= 1) {
-    if (rot & b) {
-      uint32_t t[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) t[k] = w[(k - b) & 15];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) w[k] = t[k];
-    }
-  }
+  for (int t = 0; t < 4; ++t) b[t] = __float_as_uint(fmaf(x[t], inv, kRoundMagic));
+  const uint32_t t01 = __byte_perm(b[0], b[1], 0x5140);   // b0.0 b1.0 b0.1 b1.1
+  const uint32_t t23 = __byte_perm(b[2], b[3], 0x5140);
+  w0 = __byte_perm(t01, t23, 0x5410);
+  w1 = __byte_perm(t01, t23, 0x7632);
+  const uint32_t u01 = __byte_perm(b[0], b[1], 0x0062);   // b0.2 b1.2 - -
+  const uint32_t u23 = __byte_perm(b[2], b[3], 0x0062);
+  // high byte h + 0x40 in 0..127 -> h: flip bit 6, then copy bit 6 into bit 7
+  const uint32_t h = __byte_perm(u01, u23, 0x5410) ^ 0x40404040u;
+  w2 = h | ((h & 0x40404040u) << 1);
 }
 
 // Per-thread constants that select this thread's sub-blocks 2c and 2c+1.
@@ -333,53 +335,79 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
       for (int i = 0; i < C::kConsumerWarps; ++i) tot += s_red[i];
       r = 1.0f / sqrtf(tot / static_cast<float>(K) + eps);
     }
-    // This thread's 64 activations: sub-block 2c (x_lo, chunks 0..7 of four) and
-    // 2c+1 (x_hi, chunks 8..15).  Thread u's 64 columns start 256 B after
-    // thread u-1's, so in natural order every lane of a warp would read the same
-    // shared-memory banks; lane l reads its chunks in the order (i + l) mod 16,
-    // l taken mod 8 (the eight lanes of each quarter-warp then cover all banks),
-    // does all elementwise work in that order and rotates the finished plane
-    // words back.
+    // This thread's activations: unit u = (kb, c) covers 64 columns, sub-block
+    // 2c (x_lo, natural chunks 0..7 of four columns) and 2c+1 (x_hi, chunks
+    // 8..15).  The unit's four threads (one per stream) each load and quantise
+    // one quarter (four chunks): quarter q = (stream + u) mod 4, chunk order
+    // rotated by (u / 2) mod 4, which puts the eight lanes of every
+    // quarter-warp on distinct shared-memory banks.
     XPlanes xl, xh;
-    float sx_lo = 0.0f, sx_hi = 0.0f, sigma_half;
+    float sx_lo, sx_hi, sigma_half;
     {
-      const int rot = lane & 7;
-      const int col = kb * kBlockWeights + 64 * c;
-      float xv[16][4];
+      const int q = (stream + u) & 3;
+      const int rot = (u >> 1) & 3;
+      const int base = kb * kBlockWeights + 64 * c + 16 * q;
+      float xv[4][4];
+      float amax = 0.0f, psum = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int gch = (i + rot) & 15;                   // chunk in natural order
-        const int off = col + 32 * (gch >> 3) + 4 * (gch & 7);
+      for (int i = 0; i < 4; ++i) {
+        const int off = base + 4 * ((i + rot) & 3);
         float4 h = *reinterpret_cast<const float4 *>(s_hidden + off);
         if (gamma) {
           const float4 g = *reinterpret_cast<const float4 *>(s_gamma + off);
           h = make_float4(h.x * r * g.x, h.y * r * g.y, h.z * r * g.z, h.w * r * g.w);
         }
         xv[i][0] = h.x; xv[i][1] = h.y; xv[i][2] = h.z; xv[i][3] = h.w;
+        psum += (h.x + h.y) + (h.z + h.w);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
       }
-      float amax = 0.0f;
+      // every consumer has read the staged row: its space is reused from here
+      ptx::named_bar_sync(1, C::kConsumers);
+      float2 *s_ex = reinterpret_cast<float2 *>(stages + (C::kStages - 1) * C::kStageBytes);
+      uint32_t *s_pl = reinterpret_cast<uint32_t *>(stages + (C::kStages - 1) * C::kStageBytes + C::kPlaneOffset) +
+                       u * C::kPlaneStride;
+      s_ex[u * 4 + q] = make_float2(amax, psum);
+      ptx::named_bar_sync(1, C::kConsumers);
+      const float4 e01 = *reinterpret_cast<const float4 *>(s_ex + u * 4);
+      const float4 e23 = *reinterpret_cast<const float4 *>(s_ex + u * 4 + 2);
+      const float umax = fmaxf(fmaxf(e01.x, e01.z), fmaxf(e23.x, e23.z));
+      sx_lo = e01.y + e01.w;                 // quarters 0 and 1
+      sx_hi = e23.y + e23.w;                 // quarters 2 and 3
+      const float inv = umax > 0.0f ? kQuantMax / umax : 0.0f;
+      sigma_half = umax > 0.0f ? 0.5f / inv : 0.0f;   // the 1/2 undoes the 2q form of the high nibbles
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float cs = (xv[i][0] + xv[i][1]) + (xv[i][2] + xv[i][3]);
-        if (((i + rot) & 15) < 8) sx_lo += cs; else sx_hi += cs;
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(xv[i][0]), fabsf(xv[i][1])), fmaxf(fabsf(xv[i][2]), fabsf(xv[i][3]))));
+      for (int i = 0; i < 4; ++i) {
+        uint32_t w2, w1, w0;
+        quantize_chunk(xv[i], inv, w2, w1, w0);
+        const int ch = 4 * q + ((i + rot) & 3);           // natural chunk
+        s_pl[ch] = w2;
+        s_pl[16 + ch] = w1;
+        s_pl[32 + ch] = w0;
       }
-      // every staged value has been consumed: this warp no longer reads the staging area
+      ptx::named_bar_sync(1, C::kConsumers);
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const uint4 a2 = *reinterpret_cast<const uint4 *>(s_pl + 4 * m);
+        const uint4 a1 = *reinterpret_cast<const uint4 *>(s_pl + 16 + 4 * m);
+        const uint4 a0 = *reinterpret_cast<const uint4 *>(s_pl + 32 + 4 * m);
+        const uint4 b2 = *reinterpret_cast<const uint4 *>(s_pl + 8 + 4 * m);
+        const uint4 b1 = *reinterpret_cast<const uint4 *>(s_pl + 24 + 4 * m);
+        const uint4 b0 = *reinterpret_cast<const uint4 *>(s_pl + 40 + 4 * m);
+        xl.p2[4 * m] = a2.x; xl.p2[4 * m + 1] = a2.y; xl.p2[4 * m + 2] = a2.z; xl.p2[4 * m + 3] = a2.w;
+        xl.p1[4 * m] = a1.x; xl.p1[4 * m + 1] = a1.y; xl.p1[4 * m + 2] = a1.z; xl.p1[4 * m + 3] = a1.w;
+        xl.p0[4 * m] = a0.x; xl.p0[4 * m + 1] = a0.y; xl.p0[4 * m + 2] = a0.z; xl.p0[4 * m + 3] = a0.w;
+        xh.p2[4 * m] = b2.x; xh.p2[4 * m + 1] = b2.y; xh.p2[4 * m + 2] = b2.z; xh.p2[4 * m + 3] = b2.w;
+        xh.p1[4 * m] = b1.x; xh.p1[4 * m + 1] = b1.y; xh.p1[4 * m + 2] = b1.z; xh.p1[4 * m + 3] = b1.w;
+        xh.p0[4 * m] = b0.x; xh.p0[4 * m + 1] = b0.y; xh.p0[4 * m + 2] = b0.z; xh.p0[4 * m + 3] = b0.w;
+      }
+      // release the staging stage once every word loaded from it is in a
+      // register: the move below consumes one word of each load, so it (and
+      // the arrive after it) waits for all of them
+      uint32_t dep = (xl.p2[0] ^ xl.p2[4]) ^ (xl.p1[0] ^ xl.p1[4]) ^ (xl.p0[0] ^ xl.p0[4]) ^
+                     (xh.p2[0] ^ xh.p2[4]) ^ (xh.p1[0] ^ xh.p1[4]) ^ (xh.p0[0] ^ xh.p0[4]);
+      asm volatile("mov.b32 %0, %0;" : "+r"(dep));
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(pro_done);
-      const float inv = amax > 0.0f ? kQuantMax / amax : 0.0f;
-      sigma_half = amax > 0.0f ? 0.5f / inv : 0.0f;   // the 1/2 undoes the 2q form of the high nibbles
-      uint32_t w2[16], w1[16], w0[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) quantize_chunk(xv[i], inv, w2[i], w1[i], w0[i]);
-      rotate16_right(w2, rot);
-      rotate16_right(w1, rot);
-      rotate16_right(w0, rot);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        xl.p2[i] = w2[i]; xl.p1[i] = w1[i]; xl.p0[i] = w0[i];
-        xh.p2[i] = w2[8 + i]; xh.p1[i] = w1[8 + i]; xh.p0[i] = w0[8 + i];
-      }
     }
     const UnitSel us = make_unit_sel(c);
 
