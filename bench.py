@@ -184,13 +184,15 @@ def run_reference(args, wl):
     ws, rank, _ = _dist()
     if rank != 0:
         return
-    hidden, gamma, wq = synth.inputs_for(wl)
+    group = isinstance(wl, synth.GroupWorkload)
+    hidden, gamma, wq = synth.group_inputs(wl) if group else synth.inputs_for(wl)
+    rate_fn = _oracle_rate_group if group else _oracle_rate
     per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        _oracle_rate(wl, hidden, gamma, wq, per_step * 0.2)
+        rate_fn(wl, hidden, gamma, wq, per_step * 0.2)
     rates, rows_l, secs_l, cores, reps = [], [], [], 1, 1
     for _ in range(args.steps):
-        r, rows, reps, cores, secs = _oracle_rate(wl, hidden, gamma, wq, per_step)
+        r, rows, reps, cores, secs = rate_fn(wl, hidden, gamma, wq, per_step)
         rates.append(r)
         rows_l.append(rows)
         secs_l.append(secs)
@@ -214,6 +216,12 @@ METRIC = "Q5_K LM-head forward us and achieved HBM GB/s (% of GB300 peak), batch
 
 
 def _config(wl, ws, l2_mode):
+    import q5k_synth as synth
+    if isinstance(wl, synth.GroupWorkload):
+        return {"workload": wl.name, "matrices": [[n, r] for (n, r, _, _, _) in wl.segments], "k": wl.k,
+                "batch": 1, "weights": "Q5_K 176 B / 256 weights", "norm": wl.norm,
+                "scale_cap": [[sc, cp] for (_, _, _, sc, cp) in wl.segments], "launches": 1, "l2": l2_mode,
+                "parallelism": f"replicas x{ws}"}
     return {"workload": wl.name, "n_rows": wl.n_rows, "k": wl.k, "batch": wl.batch,
             "weights": "Q5_K 176 B / 256 weights", "final_norm": wl.norm, "scale": wl.scale, "cap": wl.cap,
             "argmax": wl.argmax, "l2": l2_mode, "parallelism": f"replicas x{ws}"}
@@ -274,6 +282,51 @@ def _graph_times(fwd, stream, steps, l2_flush):
     return {"us_per_forward_median": round(statistics.median(per), 2), "steps": steps}
 
 
+def _e2e_group(args, wl, head, hidden, segs, g_d, eps, stream, nbytes):
+    """The grouped forward end to end: pinned hidden row copied in, every
+    matrix's output copied out to pinned host buffers, stream synchronised."""
+    import torch
+    h_pin = torch.from_numpy(hidden).pin_memory()
+    h_dev = torch.empty(h_pin.shape, dtype=torch.float32, device=segs[0][0].device)
+    o_pin = [torch.empty((n,), dtype=torch.float32, pin_memory=True) for (_, n, _, _, _) in segs]
+    steps = max(3, min(args.steps, 50))
+
+    def step():
+        with torch.cuda.stream(stream):
+            h_dev.copy_(h_pin, non_blocking=True)
+            outs = head.forward_group(h_dev, segs, g_d, eps, stream)
+            for o_h, o_d in zip(o_pin, outs):
+                o_h.copy_(o_d, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    secs = (time.perf_counter() - t0) / steps
+    value, secs = replica_aggregate(secs, nbytes, h_dev.device)
+    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": wl.k * 4,
+            "d2h_bytes_per_step": wl.n_rows * 4, "us_per_forward": round(secs * 1e6, 2)}
+
+
+def _oracle_rate_group(g, hidden, gamma, wqs, target_s: float):
+    """The oracle, as it stands, over every matrix of a group, whole passes for
+    `target_s` seconds.  Returns (bytes_per_s, rows, reps, cores, secs)."""
+    import oracle
+    cores = oracle.default_threads()
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        for w, (_, n, _, sc, cp) in zip(wqs, g.segments):
+            oracle.lmhead(hidden, gamma, w, sc, cp, nthreads=cores)
+        reps += 1
+        secs = time.perf_counter() - t0
+        if secs >= target_s:
+            break
+    return g.algorithmic_bytes() * reps / secs, g.n_rows, reps, cores, secs
+
+
 def run_ours(args, wl):
     import numpy as np
     import torch
@@ -293,15 +346,25 @@ def run_ours(args, wl):
         torch.distributed.barrier()
     mlh.load_library()
 
-    hidden, gamma, wq = synth.inputs_for(wl)
-    h_d = torch.from_numpy(hidden).to(dev)
-    g_d = None if gamma is None else torch.from_numpy(gamma).to(dev)
-    w_d = torch.from_numpy(wq).to(dev)
-    head = mlh.LMHead(wl.n_rows, wl.k, max_batch=wl.batch, device=local)
-    logits = torch.empty((wl.batch, wl.n_rows), dtype=torch.float32, device=dev)
-    amax = torch.empty((wl.batch,), dtype=torch.int32, device=dev) if wl.argmax else None
+    group = isinstance(wl, synth.GroupWorkload)
     stream = torch.cuda.Stream(dev)
     eps = synth.RMS_EPS
+    if group:
+        hidden, gamma, wq = synth.group_inputs(wl)     # wq: one weight matrix per segment
+        w_d = [torch.from_numpy(w).to(dev) for w in wq]
+        head = mlh.LMHead(1, wl.k, max_batch=1, device=local)
+        outs = [torch.empty((n,), dtype=torch.float32, device=dev) for (_, n, _, _, _) in wl.segments]
+        segs = [(w, n, sc, cp, o) for w, o, (_, n, _, sc, cp) in zip(w_d, outs, wl.segments)]
+        path, launches = "gemv_b1_group", 1
+    else:
+        hidden, gamma, wq = synth.inputs_for(wl)
+        w_d = torch.from_numpy(wq).to(dev)
+        head = mlh.LMHead(wl.n_rows, wl.k, max_batch=wl.batch, device=local)
+        logits = torch.empty((wl.batch, wl.n_rows), dtype=torch.float32, device=dev)
+        amax = torch.empty((wl.batch,), dtype=torch.int32, device=dev) if wl.argmax else None
+        path, launches = head.path_name(wl.batch), head.launches_per_forward(wl.batch, wl.norm)
+    h_d = torch.from_numpy(hidden).to(dev)
+    g_d = None if gamma is None else torch.from_numpy(gamma).to(dev)
     big = wl.algorithmic_bytes() > 2 * L2_BYTES
     l2_mode = ("inputs larger than L2 (weights stream from HBM every forward)" if big else
                "L2 flushed before every timed forward (256 MiB write, then a 256 MiB read so that no "
@@ -314,7 +377,10 @@ def run_ours(args, wl):
         evict.sum()
 
     def fwd():
-        head.forward(h_d, w_d, g_d, eps, wl.scale, wl.cap, wl.argmax, logits, amax, stream)
+        if group:
+            head.forward_group(h_d, segs, g_d, eps, stream)
+        else:
+            head.forward(h_d, w_d, g_d, eps, wl.scale, wl.cap, wl.argmax, logits, amax, stream)
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -364,7 +430,8 @@ def run_ours(args, wl):
     # end to end through the host-buffer entry point: pinned hidden in, logits + argmax out
     e2e = None
     if not args.no_e2e:
-        e2e = _e2e(args, wl, head, hidden, w_d, g_d, eps, stream, ws, nbytes)
+        e2e = (_e2e_group(args, wl, head, hidden, segs, g_d, eps, stream, nbytes) if group else
+               _e2e(args, wl, head, hidden, w_d, g_d, eps, stream, ws, nbytes))
 
     peak, peak_kind = _measured_peaks()
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
@@ -380,20 +447,21 @@ def run_ours(args, wl):
         "cuda_graph": graph,
         "logits_per_s": round(ws * wl.batch * wl.n_rows / (step_ms * 1e-3), 1),
         "pct_of_peak": round(100.0 * achieved / peak, 2),
-        "kernel_path": head.path_name(wl.batch),
+        "kernel_path": path,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": _profiled_traffic(head.path_name(wl.batch), wl.name),
+                     "traffic": _profiled_traffic(path, wl.name),
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "kernel": head.path_name(wl.batch),
-                     "algorithmic_bytes_per_launch": nbytes if head.launches_per_forward(wl.batch, wl.norm) == 1 else None},
+                     "kernel": path,
+                     "algorithmic_bytes_per_launch": nbytes if launches == 1 else None},
         "e2e": e2e,
-        "gpu_launches": head.launches_per_forward(wl.batch, wl.norm) * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "device_status": status,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, rows, reps, cores, secs = _oracle_rate(wl, hidden, gamma, wq, args.cpu_seconds)
+        rate, rows, reps, cores, secs = (_oracle_rate_group if group else _oracle_rate)(
+            wl, hidden, gamma, wq, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(rate / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{rows} of {wl.n_rows} weight rows x batch {wl.batch}, {reps} pass(es), "
                                           f"{secs:.1f} s wall on {cores} threads"}
@@ -411,7 +479,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="lmhead_b1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="lmhead_b1", choices=sorted(synth.WORKLOADS) + sorted(synth.GROUPS))
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -421,7 +489,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    wl = synth.WORKLOADS[args.workload]
+    wl = synth.GROUPS[args.workload] if args.workload in synth.GROUPS else synth.WORKLOADS[args.workload]
+    if args.rows and isinstance(wl, synth.GroupWorkload):
+        ap.error("--rows applies to single-matrix workloads")
     if args.rows:
         import dataclasses
         wl = dataclasses.replace(wl, name=f"{wl.name}[rows={args.rows}]", n_rows=args.rows,

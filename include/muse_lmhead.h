@@ -30,9 +30,10 @@
  *     returns a negative status and launches nothing.  Nothing aborts, traps or
  *     prints.  Asynchronous device faults surface on the caller's next
  *     synchronisation, as usual in CUDA.
- *   - A handle keeps a small device workspace (argmax partial keys and a
- *     completion counter, and split-K partial sums for short matrices).  Two
- *     forwards that may run at the same time on the GPU must use two handles.
+ *   - A handle keeps a small device workspace (argmax partial keys, a
+ *     completion counter, a status word, and the batched paths' normalised
+ *     inputs).  Two forwards that may run at the same time on the GPU must use
+ *     two handles.
  */
 #ifndef MUSE_LMHEAD_H
 #define MUSE_LMHEAD_H
@@ -152,6 +153,47 @@ int muse_lmhead_forward_b1_noalloc(int device, const float *hidden,
                                    int64_t k, float scale, float cap,
                                    float *logits, int32_t *argmax,
                                    void *stream);
+
+/*
+ * One matrix of a grouped forward (muse_lmhead_forward_group).
+ *   weights  Q5_K blocks, device, n_rows * (k/256) * 176 bytes, 16-byte aligned.
+ *   n_rows   1 .. 2^31-1.
+ *   out      [n_rows] f32, device, 4-byte aligned, written:
+ *            out[i] = cap > 0 ? cap * tanh(raw[i] * scale / cap) : raw[i] * scale.
+ */
+typedef struct muse_gemv_segment {
+  const void *weights;
+  int64_t n_rows;
+  float *out;
+  float scale;
+  float cap;
+} muse_gemv_segment;
+
+/* Largest number of matrices in one grouped forward. */
+#define MUSE_MAX_SEGMENTS 4
+
+/*
+ * Batch-1 forward of up to MUSE_MAX_SEGMENTS weight matrices that share one
+ * input row, in one launch: the input is normalised once (the same RMSNorm as
+ * muse_lmhead_forward: x = hidden * r * gamma, or x = hidden when gamma is
+ * NULL) and every matrix s writes segments[s].out = its matvec with x, scaled
+ * and capped with its own scale and cap.  No argmax.  This is the pages'
+ * concurrent group of the Q, K, V and attention-gate projections that share
+ * the attention block's normed input ("Chapter 9 — The Muse Glimmer
+ * architecture", Figure 9.1 and §9.8: Q and gate [6656 -> 4096], K and V
+ * [6656 -> 256]).
+ *   h         a handle; only its k (4,096 or 6,656, else MUSE_ERR_SHAPE), its
+ *             device and its status word are used.
+ *   hidden    [k] f32, device, 16-byte aligned.
+ *   gamma     [k] f32, device, 16-byte aligned, or NULL; eps as for forward.
+ *   segments  host array of n_segments (1..MUSE_MAX_SEGMENTS) descriptions.
+ * Validation fails closed as for muse_lmhead_forward; outputs must not overlap
+ * each other or the inputs.  Bit 0 of the handle's status word reports a
+ * bounded wait that gave up, as for forward.
+ */
+int muse_lmhead_forward_group(muse_lmhead *h, const float *hidden, const float *gamma,
+                              float eps, const muse_gemv_segment *segments,
+                              int n_segments, void *stream);
 
 /* Free the handle and its workspace.  NULL is allowed.  Must not be called
  * while a forward using the handle may still be running on the GPU. */

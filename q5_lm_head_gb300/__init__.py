@@ -19,6 +19,7 @@ __all__ = [
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
+    "muse_lmhead_forward_group", "MuseGemvSegment", "MUSE_MAX_SEGMENTS",
     "EXPORTED_SYMBOLS",
     "LOGIT_SCALE", "SOFTCAP", "RMS_EPS",
 ]
@@ -37,13 +38,21 @@ EXPORTED_SYMBOLS = (
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
+    "muse_lmhead_forward_group",
 )
 
 MUSE_OK = 0
 MUSE_MAX_BATCH = 32
+MUSE_MAX_SEGMENTS = 4
 STATUS_WAIT_TIMEOUT = 1
 
 _lib = None
+
+
+class MuseGemvSegment(ctypes.Structure):
+    """struct muse_gemv_segment of the C header: one matrix of a grouped forward."""
+    _fields_ = [("weights", ctypes.c_void_p), ("n_rows", ctypes.c_int64), ("out", ctypes.c_void_p),
+                ("scale", ctypes.c_float), ("cap", ctypes.c_float)]
 
 
 class MuseError(RuntimeError):
@@ -85,6 +94,8 @@ def load_library():
     lib.muse_lmhead_status_string.argtypes = [i32]
     lib.muse_lmhead_forward_b1_noalloc.restype = i32
     lib.muse_lmhead_forward_b1_noalloc.argtypes = [i32, vp, vp, f32, vp, i64, i64, f32, f32, vp, vp, vp]
+    lib.muse_lmhead_forward_group.restype = i32
+    lib.muse_lmhead_forward_group.argtypes = [vp, vp, vp, f32, ctypes.POINTER(MuseGemvSegment), i32, vp]
     _lib = lib
     return lib
 
@@ -147,6 +158,15 @@ def muse_lmhead_status_string(status: int) -> str:
 
 
 # ------------------------------------------------------------ torch-facing wrapper
+def muse_lmhead_forward_group(h: int | None, hidden: int, gamma: int | None, eps: float, segments,
+                              stream: int | None) -> int:
+    """segments: sequence of (weights_ptr, n_rows, out_ptr, scale, cap)."""
+    arr = (MuseGemvSegment * max(1, len(segments)))()
+    for i, (w, n, o, sc, cp) in enumerate(segments):
+        arr[i] = MuseGemvSegment(w, n, o, sc, cp)
+    return load_library().muse_lmhead_forward_group(h, hidden, gamma, eps, arr, len(segments), stream)
+
+
 class LMHead:
     """A handle for one [n_rows x k] Q5_K matrix and batches up to max_batch."""
 
@@ -229,6 +249,32 @@ class LMHead:
         if st != MUSE_OK:
             raise MuseError(st, "muse_lmhead_forward_host")
         return logits_host, argmax_host
+
+    def forward_group(self, hidden, segments, gamma=None, eps: float = RMS_EPS, stream=None):
+        """Up to four matrices against one input row in one launch.
+
+        hidden [k] (or [1, k]) f32 on the GPU; segments: sequence of
+        (weights uint8 tensor, n_rows, scale, cap, out or None).  Returns the
+        list of outputs ([n_rows] f32 each)."""
+        import torch
+        h = hidden.reshape(-1)
+        hp = self._check(h, "hidden", torch.float32, (self.k,))
+        gp = None if gamma is None else self._check(gamma, "gamma", torch.float32, (self.k,))
+        outs, descs = [], []
+        for (w, n, scale, cap, out) in segments:
+            wp = self._check(w, "weights", torch.uint8)
+            if w.numel() != n * (self.k // 256) * 176:
+                raise ValueError("weights: wrong number of bytes for n_rows")
+            if out is None:
+                out = torch.empty((n,), dtype=torch.float32, device=hidden.device)
+            op = self._check(out, "out", torch.float32, (n,))
+            outs.append(out)
+            descs.append((wp, n, op, float(scale), float(cap)))
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        st = muse_lmhead_forward_group(self.handle, hp, gp, float(eps), descs, s.cuda_stream)
+        if st != MUSE_OK:
+            raise MuseError(st, "muse_lmhead_forward_group")
+        return outs
 
     def path_name(self, batch: int) -> str | None:
         return muse_lmhead_path_name(self.handle, batch)

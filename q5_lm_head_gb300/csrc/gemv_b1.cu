@@ -3,6 +3,12 @@
 // one persistent launch ("Chapter 20 — Final norm, LM head, and the soft cap",
 // §20.1 what it computes, §20.3 the 924.6 MB weight stream, §20.4 the cap).
 //
+// The same kernel also runs a group of up to four matrices against one normed
+// input in one launch (the Q/K/V/gate projections, "Chapter 9 — The Muse
+// Glimmer architecture", Figure 9.1 and §9.8): the weight tiles of all
+// matrices form one sequence, each tile belongs to one matrix and writes that
+// matrix's output with its own scale and cap.
+//
 // Warp roles (one CTA per SM)
 //   * consumer warps: thread (kb, c) owns 64 columns, block kb, sub-blocks 2c
 //     and 2c+1, for the whole launch (column-stationary).  Four teams of such
@@ -174,11 +180,44 @@ __device__ __forceinline__ float unit_partial(const uint8_t *blk, const UnitSel 
   return fmaf(dd.x * sigma_half, dotv, -dd.y * mins);
 }
 
-template <int NB>
+// The matrices of one launch: tiles [tile_end[s-1], tile_end[s]) belong to
+// matrix s (tile_end[-1] = 0).
+struct SegTable {
+  GemvSegment seg[kMaxSegments];
+  int64_t tile_end[kMaxSegments];
+  int n;
+};
+
+// Where global tile `tile` lives: its matrix, its first row there and its rows.
+struct TileLoc {
+  int s;
+  int64_t r0;
+  int rows;
+};
+
+template <bool kGroup>
+__device__ __forceinline__ TileLoc locate(const SegTable &T, int64_t tile) {
+  TileLoc L;
+  L.s = 0;
+  int64_t t0 = 0;
+  if constexpr (kGroup) {
+#pragma unroll
+    for (int i = 1; i < kMaxSegments; ++i)
+      if (i < T.n && tile >= T.tile_end[i - 1]) {
+        L.s = i;
+        t0 = T.tile_end[i - 1];
+      }
+  }
+  L.r0 = (tile - t0) * kRows;
+  const int64_t n_rows = T.seg[L.s].n_rows;
+  L.rows = n_rows - L.r0 < kRows ? static_cast<int>(n_rows - L.r0) : kRows;
+  return L;
+}
+
+template <int NB, bool kGroup>
 __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
     gemv_b1_kernel(const float *__restrict__ hidden, const float *__restrict__ gamma, float eps,
-                   const uint8_t *__restrict__ w, int64_t n_rows, float scale, float cap,
-                   float *__restrict__ logits, unsigned long long *keys, unsigned int *ticket,
+                   const __grid_constant__ SegTable segs, unsigned long long *keys, unsigned int *ticket,
                    int32_t *argmax, uint32_t *status) {
   using C = B1Cfg<NB>;
   constexpr int K = NB * kBlockWeights;
@@ -198,7 +237,7 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int64_t n_tiles = (n_rows + kRows - 1) / kRows;
+  const int64_t n_tiles = segs.tile_end[segs.n - 1];
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -238,7 +277,8 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
     unsigned long long best = 0ull;
     // finish the rows of local tile j (its consumers have released its stage)
     auto finish = [&](int j) {
-      const int64_t r0 = (blockIdx.x + static_cast<int64_t>(j) * gridDim.x) * kRows;
+      const TileLoc L = locate<kGroup>(segs, blockIdx.x + static_cast<int64_t>(j) * gridDim.x);
+      const GemvSegment &G = segs.seg[L.s];
       const float *pr = slots + (j % C::kSlots) * (C::kSlotBytes / 4) + er * NB;
       float sacc = 0.0f;
       if (er < kRows) {
@@ -247,11 +287,11 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
           if (g + eq < NB) sacc += pr[g + eq];
       }
       sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
-      if (eq == 0 && er < kRows && r0 + er < n_rows) {
-        const int64_t row = r0 + er;
-        const float out = scale_softcap(sacc, scale, cap);
-        logits[row] = out;
-        best = umax64(best, argmax_key(out, static_cast<uint32_t>(row)));
+      if (eq == 0 && er < L.rows) {
+        const int64_t row = L.r0 + er;
+        const float out = scale_softcap(sacc, G.scale, G.cap);
+        G.out[row] = out;
+        if constexpr (!kGroup) best = umax64(best, argmax_key(out, static_cast<uint32_t>(row)));
       }
       __syncwarp();
     };
@@ -281,12 +321,12 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
         }
       }
       if (lane == 0) {
-        const int64_t r0 = (blockIdx.x + static_cast<int64_t>(j) * gridDim.x) * kRows;
-        const int rows = n_rows - r0 < kRows ? static_cast<int>(n_rows - r0) : kRows;
-        const uint32_t bytes = static_cast<uint32_t>(rows * C::kRowBytes);
+        const TileLoc L = locate<kGroup>(segs, blockIdx.x + static_cast<int64_t>(j) * gridDim.x);
+        const uint32_t bytes = static_cast<uint32_t>(L.rows * C::kRowBytes);
         const int st = j % C::kStages;
         ptx::mbar_arrive_expect_tx(&full[st], bytes);
-        ptx::bulk_g2s(stages + st * C::kStageBytes, w + r0 * C::kRowBytes, bytes, &full[st], policy);
+        ptx::bulk_g2s(stages + st * C::kStageBytes, segs.seg[L.s].w + L.r0 * C::kRowBytes, bytes, &full[st],
+                      policy);
       }
       if (j >= C::kStages) finish(j - C::kStages);
     }
@@ -420,8 +460,7 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
         if (lane == 0) fail();
         break;
       }
-      const int64_t r0 = tile * kRows;
-      const int rows = n_rows - r0 < kRows ? static_cast<int>(n_rows - r0) : kRows;
+      const int rows = locate<kGroup>(segs, tile).rows;
       float *slot = slots + ps * (C::kSlotBytes / 4) + kb;
       const uint8_t *sbase = stages + st * C::kStageBytes + kb * kBlockBytes;
       float pv[kRows / kStreams];
@@ -456,8 +495,10 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
   if (argmax) argmax_publish_finish(keys, ticket, argmax, s_best, 1);
 }
 
-template <int NB>
-cudaError_t launch_b1_nb(const LaunchArgs &a) {
+template <int NB, bool kGroup>
+cudaError_t launch_b1_nb(const float *hidden, const float *gamma, float eps, const SegTable &T,
+                         unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status,
+                         int num_sms, cudaStream_t stream) {
   using C = B1Cfg<NB>;
   static unsigned long long configured = 0;   // one bit per device: the attribute is per device
   int dev = 0;
@@ -465,16 +506,28 @@ cudaError_t launch_b1_nb(const LaunchArgs &a) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured & bit)) {
-    e = cudaFuncSetAttribute(gemv_b1_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    e = cudaFuncSetAttribute(gemv_b1_kernel<NB, kGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
-  const int64_t n_tiles = (a.n_rows + kRows - 1) / kRows;
-  const int64_t grid = n_tiles < a.num_sms ? n_tiles : a.num_sms;
-  gemv_b1_kernel<NB><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, a.stream>>>(
-      a.hidden, a.gamma, a.eps, a.w, a.n_rows, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket,
-      a.argmax, a.ws.status);
+  const int64_t n_tiles = T.tile_end[T.n - 1];
+  const int64_t grid = n_tiles < num_sms ? n_tiles : num_sms;
+  gemv_b1_kernel<NB, kGroup><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
+      hidden, gamma, eps, T, keys, ticket, argmax, status);
   return cudaGetLastError();
+}
+
+SegTable make_table(const GemvSegment *segs, int n) {
+  SegTable T = {};
+  int64_t end = 0;
+  for (int i = 0; i < n; ++i) {
+    T.seg[i] = segs[i];
+    end += (segs[i].n_rows + kRows - 1) / kRows;
+    T.tile_end[i] = end;
+  }
+  T.n = n;
+  return T;
 }
 
 }  // namespace
@@ -482,9 +535,26 @@ cudaError_t launch_b1_nb(const LaunchArgs &a) {
 bool b1_supported(int k) { return k == 26 * kBlockWeights || k == 16 * kBlockWeights; }
 
 cudaError_t launch_b1(const LaunchArgs &a) {
+  const GemvSegment one = {a.w, a.logits, a.n_rows, a.scale, a.cap};
+  const SegTable T = make_table(&one, 1);
   switch (a.k / kBlockWeights) {
-    case 26: return launch_b1_nb<26>(a);
-    case 16: return launch_b1_nb<16>(a);
+    case 26: return launch_b1_nb<26, false>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
+                                            a.ws.status, a.num_sms, a.stream);
+    case 16: return launch_b1_nb<16, false>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
+                                            a.ws.status, a.num_sms, a.stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_b1_group(const float *hidden, const float *gamma, float eps, int k, const GemvSegment *segs,
+                            int n, uint32_t *status, int num_sms, cudaStream_t stream) {
+  if (n < 1 || n > kMaxSegments) return cudaErrorInvalidValue;
+  const SegTable T = make_table(segs, n);
+  switch (k / kBlockWeights) {
+    case 26: return launch_b1_nb<26, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status, num_sms,
+                                           stream);
+    case 16: return launch_b1_nb<16, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status, num_sms,
+                                           stream);
     default: return cudaErrorInvalidValue;
   }
 }

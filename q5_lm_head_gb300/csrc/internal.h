@@ -36,10 +36,23 @@ struct LaunchArgs {
   cudaStream_t stream;
 };
 
+// One matrix of a grouped batch-1 launch: Q5_K rows `w` ([n_rows][k/256][176]),
+// output `out` ([n_rows] f32), out = cap > 0 ? cap*tanh(raw*scale/cap) : raw*scale.
+struct GemvSegment {
+  const uint8_t *w;
+  float *out;
+  int64_t n_rows;
+  float scale, cap;
+};
+constexpr int kMaxSegments = 4;
+
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_generic(const LaunchArgs &a);     // RMSNorm pre-pass (if gamma) + generic GEMV
 bool b1_supported(int k);                            // fast batch-1 kernel compiled for this K
 cudaError_t launch_b1(const LaunchArgs &a);          // fused batch-1 kernel
+// Up to kMaxSegments matrices against one normed input row, one launch (K as for b1_supported).
+cudaError_t launch_b1_group(const float *hidden, const float *gamma, float eps, int k, const GemvSegment *segs,
+                            int n, uint32_t *status, int num_sms, cudaStream_t stream);
 
 int generic_launches(const LaunchArgs &a);
 

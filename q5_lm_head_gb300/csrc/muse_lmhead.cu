@@ -166,6 +166,29 @@ int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k, i
   return MUSE_OK;
 }
 
+int muse_lmhead_forward_group(muse_lmhead *h, const float *hidden, const float *gamma, float eps,
+                              const muse_gemv_segment *segments, int n_segments, void *stream) {
+  if (!h || !hidden || !segments) return MUSE_ERR_NULL;
+  if (n_segments < 1 || n_segments > MUSE_MAX_SEGMENTS) return MUSE_ERR_SHAPE;
+  if (!muse::b1_supported(static_cast<int>(h->k))) return MUSE_ERR_SHAPE;
+  if (gamma && (!std::isfinite(eps) || eps < 0.0f)) return MUSE_ERR_VALUE;
+  if (!aligned(hidden, 16) || (gamma && !aligned(gamma, 16))) return MUSE_ERR_ALIGN;
+  muse::GemvSegment segs[muse::kMaxSegments];
+  for (int i = 0; i < n_segments; ++i) {
+    const muse_gemv_segment &g = segments[i];
+    if (!g.weights || !g.out) return MUSE_ERR_NULL;
+    if (g.n_rows < 1 || g.n_rows > (int64_t{1} << 31) - 1) return MUSE_ERR_SHAPE;
+    if (!std::isfinite(g.scale) || !std::isfinite(g.cap)) return MUSE_ERR_VALUE;
+    if (!aligned(g.weights, 16) || !aligned(g.out, 4)) return MUSE_ERR_ALIGN;
+    segs[i] = {static_cast<const uint8_t *>(g.weights), g.out, g.n_rows, g.scale, g.cap};
+  }
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return MUSE_ERR_DEVICE;
+  const cudaError_t e = muse::launch_b1_group(hidden, gamma, eps, static_cast<int>(h->k), segs, n_segments,
+                                              h->ws.status, h->num_sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
+}
+
 int muse_lmhead_forward(muse_lmhead *h, const float *hidden, int batch, const float *gamma, float eps,
                         const void *weights, float scale, float cap, float *logits, int32_t *argmax,
                         void *stream) {

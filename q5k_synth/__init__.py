@@ -233,6 +233,55 @@ for _b in (1, 2, 4, 8, 16, 32):
     WORKLOADS[f"sweep_b{_b}"] = _lm(f"sweep_b{_b}", _b)
 
 
+@dataclass(frozen=True)
+class GroupWorkload:
+    """Several Q5_K matrices against one input row in one launch.  segments:
+    ((name, n_rows, weight_tag, scale, cap), ...)."""
+    name: str
+    k: int
+    segments: tuple
+    norm: bool = True
+    hidden_tag: str = ""
+    gamma_tag: str = ""
+    batch: int = 1
+    argmax: bool = False
+
+    @property
+    def n_rows(self) -> int:
+        return sum(s[1] for s in self.segments)
+
+    @property
+    def weight_bytes(self) -> int:
+        return self.n_rows * (self.k // BLOCK_WEIGHTS) * BLOCK_BYTES
+
+    def algorithmic_bytes(self) -> int:
+        """Q5_K weights of every matrix + hidden + gamma + outputs."""
+        b = self.weight_bytes + self.k * 4 + self.n_rows * 4
+        if self.norm:
+            b += self.k * 4
+        return b
+
+
+# The attention block's concurrent group: Q and gate [6656 -> 4096], K and V
+# [6656 -> 256] from the attn_norm-normalised residual (no scale, no cap).
+GROUPS: dict[str, GroupWorkload] = {
+    "attn_qkvg": GroupWorkload("attn_qkvg", HIDDEN,
+                               (("q", 4096, "W:attn_q", 1.0, 0.0), ("gate", 4096, "W:attn_gate", 1.0, 0.0),
+                                ("k", 256, "W:attn_k", 1.0, 0.0), ("v", 256, "W:attn_v", 1.0, 0.0)),
+                               hidden_tag="H:attn_qkvg", gamma_tag="G:attn_norm"),
+}
+
+
+def group_inputs(g: GroupWorkload | str, seed: int = 0):
+    """(hidden [1, K] f32, gamma [K] f32 or None, [weights of each matrix])."""
+    if isinstance(g, str):
+        g = GROUPS[g]
+    h = normal_f64(g.k, stream_key(seed, g.hidden_tag)).reshape(1, g.k).astype(np.float32)
+    gam = normal_f64(g.k, stream_key(seed, g.gamma_tag), 1.0, 0.1).astype(np.float32) if g.norm else None
+    ws = [q5k_matrix(n, g.k, stream_key(seed, tag)) for (_, n, tag, _, _) in g.segments]
+    return h, gam, ws
+
+
 def hidden_for(w: Workload, seed: int = 0, batch: int | None = None) -> np.ndarray:
     """hidden [B, K] f32: N(0,1), each row optionally scaled by U(lo, hi), rounded once to f32."""
     b = w.batch if batch is None else batch
