@@ -151,6 +151,19 @@ def lmhead(hidden: np.ndarray, gamma: np.ndarray | None, wq: np.ndarray, scale: 
     return (out, raw) if want_raw else out
 
 
+def log_softmax(out: np.ndarray):
+    """Per row of the capped logits — softmax and logprobs are taken over the
+    logits after scale and cap ("Chapter 20 — Final norm, LM head, and the soft
+    cap", §20.7; softmax exp(x_i) / sum_j exp(x_j) as defined in "Chapter 9 —
+    The Muse Glimmer architecture") — the plain definition in f64:
+        M = max_j out_j,  lse = M + log(sum_j exp(out_j - M)),  logprob_j = out_j - lse.
+    Returns (logprobs [B, N] f64, lse [B] f64)."""
+    o = np.atleast_2d(np.asarray(out, dtype=np.float64))
+    m = o.max(axis=1, keepdims=True)
+    lse = m[:, 0] + np.log(np.exp(o - m).sum(axis=1))
+    return o - lse[:, None], lse
+
+
 def argmax_first(out: np.ndarray) -> np.ndarray:
     """Per row: the lowest index holding the row's maximum."""
     return np.argmax(np.atleast_2d(out), axis=1).astype(np.int64)

@@ -288,3 +288,34 @@ def test_byte_bill_chapter20():
     assert wl.n_rows * bill["blocks_per_row"] * 144 == bill["q4k_weight_bytes"]
     small = synth.q5k_matrix(3, wl.k, synth.stream_key(0, "pin-bill"))
     assert small.shape[1] == bill["bytes_per_row"]
+
+
+# ----------------------------------------------------------------- log-softmax over the capped logits
+def test_log_softmax_hand_cases():
+    lp, lse = oracle.log_softmax(np.array([[0.0, 0.0], [0.0, np.log(3.0)], [7.5, 7.5]]))
+    assert np.allclose(lp[0], [-np.log(2.0)] * 2, rtol=0, atol=1e-15) and abs(lse[0] - np.log(2.0)) < 1e-15
+    assert np.allclose(lp[1], [-np.log(4.0), np.log(3.0) - np.log(4.0)], rtol=0, atol=1e-15)
+    assert abs(lse[2] - (7.5 + np.log(2.0))) < 1e-14
+    lp1, lse1 = oracle.log_softmax(np.array([[-3.25]]))          # one column: probability 1
+    assert lp1[0, 0] == 0.0 and lse1[0] == -3.25
+
+
+def test_log_softmax_uniform_and_saturated_rows():
+    n = 202048
+    lp, lse = oracle.log_softmax(np.full((1, n), 20.0))         # all logits at the cap
+    assert np.allclose(lp, -np.log(n), rtol=0, atol=1e-12) and abs(lse[0] - (20.0 + np.log(n))) < 1e-12
+    lp, _ = oracle.log_softmax(np.array([[20.0, -20.0]]))       # the cap's extremes
+    assert abs(lp[0, 0] - (-np.log1p(np.exp(-40.0)))) < 1e-30
+    assert abs(lp[0, 1] - (-40.0 - np.log1p(np.exp(-40.0)))) < 1e-13
+
+
+def test_log_softmax_sums_to_one_and_is_shift_invariant():
+    rng = np.random.default_rng(21)
+    o = 20.0 * np.tanh(rng.normal(-1.6, 5.0, size=(3, 50000)) / 20.0)    # capped-logit-like rows
+    lp, lse = oracle.log_softmax(o)
+    assert np.allclose(np.exp(lp).sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    assert np.all(lp <= 0.0)
+    lp2, lse2 = oracle.log_softmax(o + 13.0)
+    assert np.allclose(lp2, lp, rtol=0, atol=1e-12) and np.allclose(lse2, lse + 13.0, rtol=0, atol=1e-12)
+    # the order of the row is kept, and the argmax has the largest logprob
+    assert np.array_equal(np.argmax(lp, axis=1), oracle.argmax_first(o))
