@@ -310,6 +310,37 @@ def _e2e_group(args, wl, head, hidden, segs, g_d, eps, stream, nbytes):
             "d2h_bytes_per_step": wl.n_rows * 4, "us_per_forward": round(secs * 1e6, 2)}
 
 
+def _e2e_logprobs(args, wl, head, hidden, w_d, g_d, eps, stream, nbytes):
+    """The logprobs forward end to end: pinned hidden rows copied in, logprobs,
+    lse and argmax copied out to pinned host buffers, stream synchronised."""
+    import torch
+    h_pin = torch.from_numpy(hidden).pin_memory()
+    h_dev = torch.empty(h_pin.shape, dtype=torch.float32, device=w_d.device)
+    lp_pin = torch.empty((wl.batch, wl.n_rows), dtype=torch.float32, pin_memory=True)
+    lse_pin = torch.empty((wl.batch,), dtype=torch.float32, pin_memory=True)
+    am_pin = torch.empty((wl.batch,), dtype=torch.int32, pin_memory=True)
+    steps = max(3, min(args.steps, 50))
+
+    def step():
+        with torch.cuda.stream(stream):
+            h_dev.copy_(h_pin, non_blocking=True)
+            lp, lse, am = head.forward_logprobs(h_dev, w_d, g_d, eps, wl.scale, wl.cap, True, stream=stream)
+            lp_pin.copy_(lp, non_blocking=True)
+            lse_pin.copy_(lse, non_blocking=True)
+            am_pin.copy_(am, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    secs = (time.perf_counter() - t0) / steps
+    value, secs = replica_aggregate(secs, nbytes, h_dev.device)
+    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": wl.batch * wl.k * 4,
+            "d2h_bytes_per_step": wl.batch * (wl.n_rows + 2) * 4, "us_per_forward": round(secs * 1e6, 2)}
+
+
 def _oracle_rate_group(g, hidden, gamma, wqs, target_s: float):
     """The oracle, as it stands, over every matrix of a group, whole passes for
     `target_s` seconds.  Returns (bytes_per_s, rows, reps, cores, secs)."""
@@ -363,6 +394,10 @@ def run_ours(args, wl):
         logits = torch.empty((wl.batch, wl.n_rows), dtype=torch.float32, device=dev)
         amax = torch.empty((wl.batch,), dtype=torch.int32, device=dev) if wl.argmax else None
         path, launches = head.path_name(wl.batch), head.launches_per_forward(wl.batch, wl.norm)
+        if args.logprobs:           # + the apply kernel (+ a pass over the logits off the fused path)
+            launches += 1 if path == "gemv_b1" else 2
+            path = path + "+logprobs"
+            lse_d = torch.empty((wl.batch,), dtype=torch.float32, device=dev)
     h_d = torch.from_numpy(hidden).to(dev)
     g_d = None if gamma is None else torch.from_numpy(gamma).to(dev)
     big = wl.algorithmic_bytes() > 2 * L2_BYTES
@@ -379,6 +414,8 @@ def run_ours(args, wl):
     def fwd():
         if group:
             head.forward_group(h_d, segs, g_d, eps, stream)
+        elif args.logprobs:
+            head.forward_logprobs(h_d, w_d, g_d, eps, wl.scale, wl.cap, wl.argmax, logits, lse_d, amax, stream)
         else:
             head.forward(h_d, w_d, g_d, eps, wl.scale, wl.cap, wl.argmax, logits, amax, stream)
 
@@ -430,8 +467,12 @@ def run_ours(args, wl):
     # end to end through the host-buffer entry point: pinned hidden in, logits + argmax out
     e2e = None
     if not args.no_e2e:
-        e2e = (_e2e_group(args, wl, head, hidden, segs, g_d, eps, stream, nbytes) if group else
-               _e2e(args, wl, head, hidden, w_d, g_d, eps, stream, ws, nbytes))
+        if group:
+            e2e = _e2e_group(args, wl, head, hidden, segs, g_d, eps, stream, nbytes)
+        elif args.logprobs:
+            e2e = _e2e_logprobs(args, wl, head, hidden, w_d, g_d, eps, stream, nbytes)
+        else:
+            e2e = _e2e(args, wl, head, hidden, w_d, g_d, eps, stream, ws, nbytes)
 
     peak, peak_kind = _measured_peaks()
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
@@ -459,6 +500,8 @@ def run_ours(args, wl):
         "clocks": clocks,
         "device_status": status,
     }
+    if not group and args.logprobs:
+        line["config"]["output"] = "logprobs: log-softmax of the capped logits, plus lse and argmax"
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, rows, reps, cores, secs = (_oracle_rate_group if group else _oracle_rate)(
             wl, hidden, gamma, wq, args.cpu_seconds)
@@ -481,6 +524,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="lmhead_b1", choices=sorted(synth.WORKLOADS) + sorted(synth.GROUPS))
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--logprobs", action="store_true",
+                    help="time the logprobs forward (log-softmax of the capped logits) instead of the logits")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -490,8 +535,8 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     wl = synth.GROUPS[args.workload] if args.workload in synth.GROUPS else synth.WORKLOADS[args.workload]
-    if args.rows and isinstance(wl, synth.GroupWorkload):
-        ap.error("--rows applies to single-matrix workloads")
+    if (args.rows or args.logprobs) and isinstance(wl, synth.GroupWorkload):
+        ap.error("--rows and --logprobs apply to single-matrix workloads")
     if args.rows:
         import dataclasses
         wl = dataclasses.replace(wl, name=f"{wl.name}[rows={args.rows}]", n_rows=args.rows,

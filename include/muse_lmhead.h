@@ -90,6 +90,25 @@ int muse_lmhead_forward(muse_lmhead *h, const float *hidden, int batch,
                         void *stream);
 
 /*
+ * The same forward, returning logprobs instead of logits: per batch row b,
+ *     lse[b]         = log sum_i exp(logits[b][i])       (log-softmax normaliser)
+ *     logprobs[b][i] = logits[b][i] - lse[b]
+ * over the logits after scale and cap — the pages take softmax and logprobs
+ * over the capped logits ("Chapter 20 — Final norm, LM head, and the soft cap",
+ * §20.7).  The logits themselves are logprobs[b][i] + lse[b].
+ *   logprobs [batch][n_rows] f32, device, 16-byte aligned, written.
+ *   lse      [batch] f32, device, 4-byte aligned, written; or NULL to skip it.
+ *   argmax   as for muse_lmhead_forward (the largest logprob's index).
+ * Other arguments and validation as for muse_lmhead_forward.  At batch 1 with
+ * the fused kernel the normaliser is accumulated in the kernel's epilogue and
+ * one more small launch subtracts it; other paths add a pass over the logits.
+ */
+int muse_lmhead_forward_logprobs(muse_lmhead *h, const float *hidden, int batch,
+                                 const float *gamma, float eps, const void *weights,
+                                 float scale, float cap, float *logprobs, float *lse,
+                                 int32_t *argmax, void *stream);
+
+/*
  * The same forward for callers whose activations live in host memory: copies
  * hidden_host to the device, runs the forward, copies the logits (and argmax)
  * back, and waits for `stream` before returning.  gamma and weights are device

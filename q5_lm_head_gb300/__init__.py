@@ -19,7 +19,7 @@ __all__ = [
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
-    "muse_lmhead_forward_group", "MuseGemvSegment", "MUSE_MAX_SEGMENTS",
+    "muse_lmhead_forward_group", "MuseGemvSegment", "MUSE_MAX_SEGMENTS", "muse_lmhead_forward_logprobs",
     "EXPORTED_SYMBOLS",
     "LOGIT_SCALE", "SOFTCAP", "RMS_EPS",
 ]
@@ -38,7 +38,7 @@ EXPORTED_SYMBOLS = (
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
-    "muse_lmhead_forward_group",
+    "muse_lmhead_forward_group", "muse_lmhead_forward_logprobs",
 )
 
 MUSE_OK = 0
@@ -94,6 +94,8 @@ def load_library():
     lib.muse_lmhead_status_string.argtypes = [i32]
     lib.muse_lmhead_forward_b1_noalloc.restype = i32
     lib.muse_lmhead_forward_b1_noalloc.argtypes = [i32, vp, vp, f32, vp, i64, i64, f32, f32, vp, vp, vp]
+    lib.muse_lmhead_forward_logprobs.restype = i32
+    lib.muse_lmhead_forward_logprobs.argtypes = [vp, vp, i32, vp, f32, vp, f32, f32, vp, vp, vp, vp]
     lib.muse_lmhead_forward_group.restype = i32
     lib.muse_lmhead_forward_group.argtypes = [vp, vp, vp, f32, ctypes.POINTER(MuseGemvSegment), i32, vp]
     _lib = lib
@@ -158,6 +160,13 @@ def muse_lmhead_status_string(status: int) -> str:
 
 
 # ------------------------------------------------------------ torch-facing wrapper
+def muse_lmhead_forward_logprobs(h: int, hidden: int, batch: int, gamma: int | None, eps: float, weights: int,
+                                 scale: float, cap: float, logprobs: int, lse: int | None, argmax: int | None,
+                                 stream: int | None) -> int:
+    return load_library().muse_lmhead_forward_logprobs(h, hidden, batch, gamma, eps, weights, scale, cap,
+                                                       logprobs, lse, argmax, stream)
+
+
 def muse_lmhead_forward_group(h: int | None, hidden: int, gamma: int | None, eps: float, segments,
                               stream: int | None) -> int:
     """segments: sequence of (weights_ptr, n_rows, out_ptr, scale, cap)."""
@@ -249,6 +258,37 @@ class LMHead:
         if st != MUSE_OK:
             raise MuseError(st, "muse_lmhead_forward_host")
         return logits_host, argmax_host
+
+    def forward_logprobs(self, hidden, weights, gamma=None, eps: float = RMS_EPS, scale: float = LOGIT_SCALE,
+                         cap: float = SOFTCAP, want_argmax: bool = True, logprobs=None, lse=None, argmax=None,
+                         stream=None):
+        """(logprobs [B, n_rows], lse [B][, argmax [B]]): log-softmax of the capped logits."""
+        import torch
+        if hidden.dim() == 1:
+            hidden = hidden.unsqueeze(0)
+        b = hidden.shape[0]
+        hp = self._check(hidden, "hidden", torch.float32, (b, self.k))
+        wp = self._check(weights, "weights", torch.uint8)
+        if weights.numel() != self.n_rows * (self.k // 256) * 176:
+            raise ValueError("weights: wrong number of bytes for this handle")
+        gp = None if gamma is None else self._check(gamma, "gamma", torch.float32, (self.k,))
+        if logprobs is None:
+            logprobs = torch.empty((b, self.n_rows), dtype=torch.float32, device=hidden.device)
+        lp = self._check(logprobs, "logprobs", torch.float32, (b, self.n_rows))
+        if lse is None:
+            lse = torch.empty((b,), dtype=torch.float32, device=hidden.device)
+        sp = self._check(lse, "lse", torch.float32, (b,))
+        ap = None
+        if want_argmax:
+            if argmax is None:
+                argmax = torch.empty((b,), dtype=torch.int32, device=hidden.device)
+            ap = self._check(argmax, "argmax", torch.int32, (b,))
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        st = muse_lmhead_forward_logprobs(self.handle, hp, b, gp, float(eps), wp, float(scale), float(cap), lp, sp,
+                                          ap, s.cuda_stream)
+        if st != MUSE_OK:
+            raise MuseError(st, "muse_lmhead_forward_logprobs")
+        return (logprobs, lse, argmax) if want_argmax else (logprobs, lse)
 
     def forward_group(self, hidden, segments, gamma=None, eps: float = RMS_EPS, stream=None):
         """Up to four matrices against one input row in one launch.

@@ -38,6 +38,40 @@ __device__ __forceinline__ void q5k_scale_min(uint32_t w0, uint32_t w1, uint32_t
   }
 }
 
+// Online (max, sum of exp) pair of a set of values: s = sum_j exp(v_j - m).
+// The empty set is (-inf, 0).  log-softmax normaliser of the set: m + log(s).
+struct MaxSum {
+  float m, s;
+};
+
+__device__ __forceinline__ MaxSum ms_empty() { return {-INFINITY, 0.0f}; }
+
+__device__ __forceinline__ MaxSum ms_add(MaxSum a, float v) {
+  if (v <= a.m) {
+    a.s += expf(v - a.m);
+  } else {
+    a.s = a.s * expf(a.m - v) + 1.0f;   // a.m = -inf: 0 * 0 + 1
+    a.m = v;
+  }
+  return a;
+}
+
+__device__ __forceinline__ MaxSum ms_combine(MaxSum a, MaxSum b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return a;         // both empty
+  return {m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
+}
+
+__device__ __forceinline__ MaxSum ms_warp_combine(MaxSum a) {
+  for (int o = 16; o > 0; o >>= 1) {
+    MaxSum b;
+    b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+    b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+    a = ms_combine(a, b);
+  }
+  return a;
+}
+
 // Total order on finite floats as unsigned keys; -0 is folded onto +0 first.
 __device__ __forceinline__ uint32_t float_order_key(float v) {
   v = v + 0.0f;

@@ -218,7 +218,7 @@ template <int NB, bool kGroup>
 __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
     gemv_b1_kernel(const float *__restrict__ hidden, const float *__restrict__ gamma, float eps,
                    const __grid_constant__ SegTable segs, unsigned long long *keys, unsigned int *ticket,
-                   int32_t *argmax, uint32_t *status) {
+                   int32_t *argmax, uint32_t *status, float2 *lse_parts) {
   using C = B1Cfg<NB>;
   constexpr int K = NB * kBlockWeights;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
   const float *s_gamma = s_hidden + K;
   unsigned long long *s_best = reinterpret_cast<unsigned long long *>(s_red + 32);
   volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(s_best + 1);
+  float2 *s_ms = reinterpret_cast<float2 *>(s_best + 2);                   // [2] producers' (max, sum exp)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
     static_assert(kRows <= 16, "two lanes per row");
     const int er = lane >> 1, eq = lane & 1;
     unsigned long long best = 0ull;
+    MaxSum ms = ms_empty();                     // log-softmax normaliser of this lane's rows
     // finish the rows of local tile j (its consumers have released its stage)
     auto finish = [&](int j) {
       const TileLoc L = locate<kGroup>(segs, blockIdx.x + static_cast<int64_t>(j) * gridDim.x);
@@ -291,7 +293,10 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
         const int64_t row = L.r0 + er;
         const float out = scale_softcap(sacc, G.scale, G.cap);
         G.out[row] = out;
-        if constexpr (!kGroup) best = umax64(best, argmax_key(out, static_cast<uint32_t>(row)));
+        if constexpr (!kGroup) {
+          best = umax64(best, argmax_key(out, static_cast<uint32_t>(row)));
+          if (lse_parts) ms = ms_add(ms, out);
+        }
       }
       __syncwarp();
     };
@@ -348,6 +353,10 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
     }
     for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
     if (lane == 0 && best != 0ull) atomicMax(s_best, best);
+    if (lse_parts) {
+      ms = ms_warp_combine(ms);
+      if (lane == 0) s_ms[pw] = make_float2(ms.m, ms.s);
+    }
   } else {
     // ------------------------------------------------------------ consumers
     const int stream = tid / C::kUnits;
@@ -492,13 +501,17 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
   }
 
   __syncthreads();
+  if (lse_parts && tid == 0) {                  // this CTA's pair, in a fixed order
+    const MaxSum c = ms_combine({s_ms[0].x, s_ms[0].y}, {s_ms[1].x, s_ms[1].y});
+    lse_parts[blockIdx.x] = make_float2(c.m, c.s);
+  }
   if (argmax) argmax_publish_finish(keys, ticket, argmax, s_best, 1);
 }
 
 template <int NB, bool kGroup>
 cudaError_t launch_b1_nb(const float *hidden, const float *gamma, float eps, const SegTable &T,
                          unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status,
-                         int num_sms, cudaStream_t stream) {
+                         float2 *lse_parts, int num_sms, cudaStream_t stream) {
   using C = B1Cfg<NB>;
   static unsigned long long configured = 0;   // one bit per device: the attribute is per device
   int dev = 0;
@@ -514,7 +527,7 @@ cudaError_t launch_b1_nb(const float *hidden, const float *gamma, float eps, con
   const int64_t n_tiles = T.tile_end[T.n - 1];
   const int64_t grid = n_tiles < num_sms ? n_tiles : num_sms;
   gemv_b1_kernel<NB, kGroup><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
-      hidden, gamma, eps, T, keys, ticket, argmax, status);
+      hidden, gamma, eps, T, keys, ticket, argmax, status, lse_parts);
   return cudaGetLastError();
 }
 
@@ -534,14 +547,20 @@ SegTable make_table(const GemvSegment *segs, int n) {
 
 bool b1_supported(int k) { return k == 26 * kBlockWeights || k == 16 * kBlockWeights; }
 
+int b1_grid(int64_t n_rows, int num_sms) {
+  const int64_t n_tiles = (n_rows + kRows - 1) / kRows;
+  return static_cast<int>(n_tiles < num_sms ? n_tiles : num_sms);
+}
+
 cudaError_t launch_b1(const LaunchArgs &a) {
   const GemvSegment one = {a.w, a.logits, a.n_rows, a.scale, a.cap};
   const SegTable T = make_table(&one, 1);
+  float2 *parts = a.lse_parts ? a.ws.lse_parts : nullptr;   // batch row 0: one pair per CTA
   switch (a.k / kBlockWeights) {
     case 26: return launch_b1_nb<26, false>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
-                                            a.ws.status, a.num_sms, a.stream);
+                                            a.ws.status, parts, a.num_sms, a.stream);
     case 16: return launch_b1_nb<16, false>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
-                                            a.ws.status, a.num_sms, a.stream);
+                                            a.ws.status, parts, a.num_sms, a.stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -551,10 +570,10 @@ cudaError_t launch_b1_group(const float *hidden, const float *gamma, float eps, 
   if (n < 1 || n > kMaxSegments) return cudaErrorInvalidValue;
   const SegTable T = make_table(segs, n);
   switch (k / kBlockWeights) {
-    case 26: return launch_b1_nb<26, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status, num_sms,
-                                           stream);
-    case 16: return launch_b1_nb<16, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status, num_sms,
-                                           stream);
+    case 26: return launch_b1_nb<26, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status, nullptr,
+                                           num_sms, stream);
+    case 16: return launch_b1_nb<16, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status, nullptr,
+                                           num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }

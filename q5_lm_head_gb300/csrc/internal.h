@@ -18,7 +18,10 @@ struct Workspace {
   uint32_t *status;          // sticky device status bits
   float *x;                  // [max_batch][k] normalised input (generic path)
   uint8_t *xpkg;             // per-block activation packages (tensor-core path)
+  float2 *lse_parts;         // [MUSE_MAX_BATCH][kMaxLseParts] (max, sum exp) partials of the logprobs
 };
+
+constexpr int kMaxLseParts = 256;
 
 struct LaunchArgs {
   const float *hidden;   // [batch][k]
@@ -34,6 +37,7 @@ struct LaunchArgs {
   int num_sms;
   Workspace ws;
   cudaStream_t stream;
+  bool lse_parts = false;    // batch-1 kernel: also write each CTA's (max, sum exp) pair
 };
 
 // One matrix of a grouped batch-1 launch: Q5_K rows `w` ([n_rows][k/256][176]),
@@ -55,6 +59,15 @@ cudaError_t launch_b1_group(const float *hidden, const float *gamma, float eps, 
                             int n, uint32_t *status, int num_sms, cudaStream_t stream);
 
 int generic_launches(const LaunchArgs &a);
+
+// Logprobs over finished logits [batch][n_rows] (in place): partial (max, sum
+// exp) pairs per chunk of each row, then logits -= lse (a programmatic
+// dependent launch of whatever wrote the logits and pairs).
+int lse_parts_for(int64_t n_rows);         // chunks per row used by launch_lse_parts
+cudaError_t launch_lse_parts(const float *logits, int batch, int64_t n_rows, float2 *parts, cudaStream_t stream);
+cudaError_t launch_logprob_apply(float *logits, int batch, int64_t n_rows, const float2 *parts, int n_parts,
+                                 float *lse, cudaStream_t stream);
+int b1_grid(int64_t n_rows, int num_sms);   // CTAs of the batch-1 kernel = its (max, sum exp) pairs
 
 // Tensor-core path (batches 2..32): activation-package prep + tcgen05 kernel.
 bool tc_supported(int batch, int k);

@@ -76,7 +76,7 @@ int validate_forward(const muse_lmhead *h, const void *hidden, int batch, const 
 
 int run_forward(muse_lmhead *h, const float *hidden, int batch, const float *gamma, float eps,
                 const void *weights, float scale, float cap, float *logits, int32_t *argmax,
-                cudaStream_t stream) {
+                cudaStream_t stream, bool lse_parts = false) {
   muse::LaunchArgs a;
   a.hidden = hidden;
   a.gamma = gamma;
@@ -92,6 +92,7 @@ int run_forward(muse_lmhead *h, const float *hidden, int batch, const float *gam
   a.num_sms = h->num_sms;
   a.ws = h->ws;
   a.stream = stream;
+  a.lse_parts = lse_parts;
   cudaError_t e;
   switch (choose_path(h, batch)) {
     case Path::B1: e = muse::launch_b1(a); break;
@@ -137,12 +138,13 @@ int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k, i
   h->max_batch = max_batch;
   h->num_sms = prop.multiProcessorCount;
 
-  // One zeroed allocation: keys | ticket | status | x | activation packages
+  // One zeroed allocation: keys | ticket | status | logprob pairs | x | activation packages
   const size_t keys_b = sizeof(unsigned long long) * MUSE_MAX_BATCH;
   const size_t misc_b = 256;
+  const size_t lse_b = sizeof(float2) * static_cast<size_t>(max_batch) * muse::kMaxLseParts;
   const size_t x_b = sizeof(float) * static_cast<size_t>(max_batch) * static_cast<size_t>(k);
   const size_t pkg_b = max_batch >= 2 ? muse::tc_workspace_bytes(static_cast<int>(k)) : 0;
-  const size_t total = keys_b + misc_b + x_b + pkg_b;
+  const size_t total = keys_b + misc_b + lse_b + x_b + pkg_b;
   void *base = nullptr;
   e = cudaMalloc(&base, total);
   if (e != cudaSuccess) {
@@ -160,8 +162,9 @@ int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k, i
   h->ws.keys = reinterpret_cast<unsigned long long *>(p);
   h->ws.ticket = reinterpret_cast<unsigned int *>(p + keys_b);
   h->ws.status = reinterpret_cast<uint32_t *>(p + keys_b + 16);
-  h->ws.x = reinterpret_cast<float *>(p + keys_b + misc_b);
-  h->ws.xpkg = pkg_b ? p + keys_b + misc_b + x_b : nullptr;
+  h->ws.lse_parts = reinterpret_cast<float2 *>(p + keys_b + misc_b);
+  h->ws.x = reinterpret_cast<float *>(p + keys_b + misc_b + lse_b);
+  h->ws.xpkg = pkg_b ? p + keys_b + misc_b + lse_b + x_b : nullptr;
   *out = h;
   return MUSE_OK;
 }
@@ -186,6 +189,31 @@ int muse_lmhead_forward_group(muse_lmhead *h, const float *hidden, const float *
   if (!dg.ok) return MUSE_ERR_DEVICE;
   const cudaError_t e = muse::launch_b1_group(hidden, gamma, eps, static_cast<int>(h->k), segs, n_segments,
                                               h->ws.status, h->num_sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
+}
+
+int muse_lmhead_forward_logprobs(muse_lmhead *h, const float *hidden, int batch, const float *gamma, float eps,
+                                 const void *weights, float scale, float cap, float *logprobs, float *lse,
+                                 int32_t *argmax, void *stream) {
+  int st = validate_forward(h, hidden, batch, gamma, eps, weights, scale, cap, logprobs, argmax);
+  if (st != MUSE_OK) return st;
+  if (!aligned(hidden, 16) || !aligned(logprobs, 16) || (lse && !aligned(lse, 4))) return MUSE_ERR_ALIGN;
+  DeviceGuard g(h->device);
+  if (!g.ok) return MUSE_ERR_DEVICE;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the batch-1 kernel leaves one (max, sum exp) pair per CTA; other paths get a pass over the logits
+  const bool fused = choose_path(h, batch) == Path::B1;
+  st = run_forward(h, hidden, batch, gamma, eps, weights, scale, cap, logprobs, argmax, s, fused);
+  if (st != MUSE_OK) return st;
+  int n_parts;
+  cudaError_t e = cudaSuccess;
+  if (fused) {
+    n_parts = muse::b1_grid(h->n_rows, h->num_sms);
+  } else {
+    n_parts = muse::lse_parts_for(h->n_rows);
+    e = muse::launch_lse_parts(logprobs, batch, h->n_rows, h->ws.lse_parts, s);
+  }
+  if (e == cudaSuccess) e = muse::launch_logprob_apply(logprobs, batch, h->n_rows, h->ws.lse_parts, n_parts, lse, s);
   return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
 }
 
