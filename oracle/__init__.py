@@ -64,6 +64,12 @@ def _load():
         lib.oracle_scale_softcap.argtypes = [dbl, dbl, dbl]
         lib.oracle_lmhead.restype = i32
         lib.oracle_lmhead.argtypes = [vp, i64, i64, vp, dbl, vp, i64, vp, i64, dbl, dbl, vp, vp, i32]
+        lib.oracle_lmhead_fmt.restype = i32
+        lib.oracle_lmhead_fmt.argtypes = lib.oracle_lmhead.argtypes + [i32]
+        lib.oracle_q4k_parse.restype = None
+        lib.oracle_q4k_parse.argtypes = [vp, vp, vp, vp, vp, vp]
+        lib.oracle_q4k_dequant.restype = None
+        lib.oracle_q4k_dequant.argtypes = [vp, vp]
         _lib = lib
     return _lib
 
@@ -112,6 +118,30 @@ def q5k_dequant_matrix(wq: np.ndarray) -> np.ndarray:
     return out
 
 
+def q4k_parse(block: np.ndarray):
+    """(d, dmin, sc[8], m[8], q[256]) of one 144-byte Q4_K block."""
+    blk = np.ascontiguousarray(block, dtype=np.uint8)
+    assert blk.size == 144
+    d = np.zeros(1, np.float64)
+    dm = np.zeros(1, np.float64)
+    sc = np.zeros(8, np.int32)
+    m = np.zeros(8, np.int32)
+    q = np.zeros(256, np.int32)
+    _load().oracle_q4k_parse(_p(blk), _p(d), _p(dm), _p(sc), _p(m), _p(q))
+    return float(d[0]), float(dm[0]), sc, m, q
+
+
+def q4k_dequant_block(block: np.ndarray) -> np.ndarray:
+    blk = np.ascontiguousarray(block, dtype=np.uint8)
+    assert blk.size == 144
+    w = np.zeros(256, np.float64)
+    _load().oracle_q4k_dequant(_p(blk), _p(w))
+    return w
+
+
+BLOCK_BYTES = {"q5_k": 176, "q4_k": 144}
+
+
 def rmsnorm(h: np.ndarray, gamma: np.ndarray | None, eps: float = 1e-5) -> np.ndarray:
     h = np.ascontiguousarray(h, dtype=np.float32)
     g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float32)
@@ -126,26 +156,27 @@ def scale_softcap(raw: float, scale: float, cap: float) -> float:
 
 def lmhead(hidden: np.ndarray, gamma: np.ndarray | None, wq: np.ndarray, scale: float,
            cap: float, eps: float = 1e-5, rows=None, want_raw: bool = False,
-           nthreads: int | None = None):
+           nthreads: int | None = None, fmt: str = "q5_k"):
     """out [B, n_out] f64 (and raw [B, n_out] if want_raw).
 
-    hidden: [B, K] f32; gamma: [K] f32 or None (no norm); wq: [N, K/256*176] uint8;
+    hidden: [B, K] f32; gamma: [K] f32 or None (no norm); wq: [N, K/256*block bytes]
+    uint8 in fmt "q5_k" (176-byte blocks) or "q4_k" (144-byte blocks);
     rows: optional list of weight rows to compute (default: all N).
     """
     hidden = np.ascontiguousarray(np.atleast_2d(hidden), dtype=np.float32)
     b, k = hidden.shape
     wq = np.ascontiguousarray(wq, dtype=np.uint8)
     n_w = wq.shape[0]
-    if wq.shape[1] * 256 != k * 176:
+    if wq.shape[1] * 256 != k * BLOCK_BYTES[fmt]:
         raise ValueError("weight row bytes do not match K")
     g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float32)
     ra = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     n_out = n_w if ra is None else ra.size
     out = np.zeros((b, n_out), np.float64)
     raw = np.zeros((b, n_out), np.float64) if want_raw else None
-    rc = _load().oracle_lmhead(_p(hidden), b, k, _p(g), float(eps), _p(wq), n_w, _p(ra), n_out,
-                               float(scale), float(cap), _p(raw), _p(out),
-                               nthreads or default_threads())
+    rc = _load().oracle_lmhead_fmt(_p(hidden), b, k, _p(g), float(eps), _p(wq), n_w, _p(ra), n_out,
+                                   float(scale), float(cap), _p(raw), _p(out),
+                                   nthreads or default_threads(), 1 if fmt == "q4_k" else 0)
     if rc != 0:
         raise RuntimeError(f"oracle_lmhead failed ({rc})")
     return (out, raw) if want_raw else out

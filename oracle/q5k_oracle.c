@@ -29,6 +29,12 @@
  * sc = (scales[s + 4] & 15) | (scales[s - 4] >> 6) << 4 and
  * m = (scales[s + 4] >> 4) | (scales[s] >> 6) << 4.
  *
+ * Q4_K (the FFN bulk's format, and the 756.5 MB alternative head of Chapter 20
+ * §20.8: 144 bytes per 256 weights): the pages give only the block size.
+ * Reading: ggml's block_q4_K — the same fp16 d, fp16 dmin and 12 scale bytes,
+ * then 128 bytes of nibbles placed as in Q5_K, no high bits; q in 0..15 and
+ * w = d * sc_s * q - dmin * m_s.
+ *
  * Build: gcc -O2 -ffp-contract=off (no fused multiply-add, so every product and
  * sum is one correctly rounded binary64 operation, identical on x86 and Arm).
  */
@@ -80,6 +86,39 @@ void oracle_q5k_parse(const uint8_t *blk, double *d, double *dmin, int *sc, int 
   }
 }
 
+/* One Q4_K block: d, dmin, the eight 6-bit scales and mins, 256 quants 0..15. */
+void oracle_q4k_parse(const uint8_t *blk, double *d, double *dmin, int *sc, int *m,
+                      int *q) {
+  *d = oracle_half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+  *dmin = oracle_half_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+  const uint8_t *scales = blk + 4;
+  const uint8_t *qs = blk + 16;
+  for (int s = 0; s < 8; ++s) {
+    if (s < 4) {
+      sc[s] = scales[s] & 63;
+      m[s] = scales[s + 4] & 63;
+    } else {
+      sc[s] = (scales[s + 4] & 15) | ((scales[s - 4] >> 6) << 4);
+      m[s] = (scales[s + 4] >> 4) | ((scales[s] >> 6) << 4);
+    }
+  }
+  for (int e = 0; e < 256; ++e) {
+    int s = e / 32, l = e % 32;
+    q[e] = (qs[32 * (s / 2) + l] >> (4 * (s & 1))) & 15;
+  }
+}
+
+/* The 256 weight values of one Q4_K block: w = d * sc_s * q - dmin * m_s. */
+void oracle_q4k_dequant(const uint8_t *blk, double *w) {
+  double d, dmin;
+  int sc[8], m[8], q[256];
+  oracle_q4k_parse(blk, &d, &dmin, sc, m, q);
+  for (int e = 0; e < 256; ++e) {
+    int s = e / 32;
+    w[e] = d * (double)sc[s] * (double)q[e] - dmin * (double)m[s];
+  }
+}
+
 /* The 256 weight values of one block: w = d * sc_s * q - dmin * m_s. */
 void oracle_q5k_dequant(const uint8_t *blk, double *w) {
   double d, dmin;
@@ -111,7 +150,8 @@ double oracle_scale_softcap(double raw, double scale, double cap) {
 
 typedef struct {
   const double *x;       /* [batch][k] normed inputs */
-  const uint8_t *w;      /* [n_rows][nb * 176] */
+  const uint8_t *w;      /* [n_rows][nb * block bytes] */
+  int q4;                /* 1: Q4_K blocks (144 bytes), 0: Q5_K (176) */
   int64_t k, nb, batch, n_rows;
   double scale, cap;
   int64_t r0, r1;        /* output rows of this worker */
@@ -125,8 +165,12 @@ static void *lm_worker(void *arg) {
   if (!wrow) return (void *)1;
   for (int64_t i = jb->r0; i < jb->r1; ++i) {
     int64_t row = jb->rows ? jb->rows[i] : i;
-    const uint8_t *src = jb->w + row * jb->nb * 176;
-    for (int64_t kb = 0; kb < jb->nb; ++kb) oracle_q5k_dequant(src + kb * 176, wrow + kb * 256);
+    const int64_t bb = jb->q4 ? 144 : 176;
+    const uint8_t *src = jb->w + row * jb->nb * bb;
+    for (int64_t kb = 0; kb < jb->nb; ++kb) {
+      if (jb->q4) oracle_q4k_dequant(src + kb * bb, wrow + kb * 256);
+      else oracle_q5k_dequant(src + kb * bb, wrow + kb * 256);
+    }
     for (int64_t b = 0; b < jb->batch; ++b) {
       const double *xb = jb->x + b * jb->k;
       double acc = 0.0;
@@ -146,10 +190,10 @@ static void *lm_worker(void *arg) {
  * order.  raw (optional) and out are [batch][n_out] binary64.
  * Returns 0, -1 on bad arguments, -2 on allocation failure.
  */
-int oracle_lmhead(const float *hidden, int64_t batch, int64_t k, const float *gamma,
-                  double eps, const uint8_t *w, int64_t n_w_rows, const int64_t *rows,
-                  int64_t n_out, double scale, double cap, double *raw, double *out,
-                  int nthreads) {
+int oracle_lmhead_fmt(const float *hidden, int64_t batch, int64_t k, const float *gamma,
+                      double eps, const uint8_t *w, int64_t n_w_rows, const int64_t *rows,
+                      int64_t n_out, double scale, double cap, double *raw, double *out,
+                      int nthreads, int q4) {
   if (!hidden || !w || !out || batch <= 0 || k <= 0 || k % 256) return -1;
   if (!rows) n_out = n_w_rows;
   if (n_out < 0) return -1;
@@ -172,6 +216,7 @@ int oracle_lmhead(const float *hidden, int64_t batch, int64_t k, const float *ga
     jb->n_rows = n_out; jb->scale = scale; jb->cap = cap; jb->rows = rows;
     jb->r0 = n_out * t / nthreads; jb->r1 = n_out * (t + 1) / nthreads;
     jb->raw = raw; jb->out = out;
+    jb->q4 = q4;
   }
   for (int t = 0; t < nthreads; ++t) {
     started[t] = nthreads > 1 && pthread_create(&th[t], NULL, lm_worker, &jobs[t]) == 0;
@@ -186,4 +231,13 @@ int oracle_lmhead(const float *hidden, int64_t batch, int64_t k, const float *ga
   }
   free(x);
   return rc;
+}
+
+/* The Q5_K stage (the LM head's format). */
+int oracle_lmhead(const float *hidden, int64_t batch, int64_t k, const float *gamma,
+                  double eps, const uint8_t *w, int64_t n_w_rows, const int64_t *rows,
+                  int64_t n_out, double scale, double cap, double *raw, double *out,
+                  int nthreads) {
+  return oracle_lmhead_fmt(hidden, batch, k, gamma, eps, w, n_w_rows, rows, n_out, scale, cap,
+                           raw, out, nthreads, 0);
 }

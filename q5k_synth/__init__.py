@@ -33,6 +33,7 @@ _lock = threading.Lock()
 _lib = None
 
 BLOCK_BYTES = 176
+BLOCK_BYTES_Q4K = 144
 BLOCK_WEIGHTS = 256
 
 
@@ -64,6 +65,8 @@ def _load():
         lib.synth_q5k_rows.restype = i32
         lib.synth_q5k_rows.argtypes = [vp, i64, i64, i64, u64, dbl, dbl, dbl, dbl, dbl,
                                        vp, vp, vp, vp, vp, i32]
+        lib.synth_q4k_rows.restype = i32
+        lib.synth_q4k_rows.argtypes = lib.synth_q5k_rows.argtypes
         lib.synth_normal_f64.restype = None
         lib.synth_normal_f64.argtypes = [vp, i64, u64, dbl, dbl]
         lib.synth_uniform_f64.restype = None
@@ -115,23 +118,29 @@ DMIN_RANGE = (0.0, 1e-3)
 
 
 def q5k_rows(n_rows: int, k: int, key: int, row_begin: int = 0, d_mult: float = 1.0,
-             with_fields: bool = False, out: np.ndarray | None = None):
-    """Rows [row_begin, row_begin + n_rows) of a Q5_K matrix with k columns.
+             with_fields: bool = False, out: np.ndarray | None = None, fmt: str = "q5_k"):
+    """Rows [row_begin, row_begin + n_rows) of a Q5_K (or, fmt="q4_k", Q4_K)
+    matrix with k columns.
 
-    Returns uint8 [n_rows, k // 256 * 176] (and Q5KFields if with_fields).
+    Returns uint8 [n_rows, k // 256 * block bytes] (and Q5KFields if with_fields;
+    q is then 0..15 for Q4_K).
     """
     if k % BLOCK_WEIGHTS:
         raise ValueError("k must be a multiple of 256")
+    if fmt not in ("q5_k", "q4_k"):
+        raise ValueError("fmt must be q5_k or q4_k")
     nb = k // BLOCK_WEIGHTS
+    bb = BLOCK_BYTES if fmt == "q5_k" else BLOCK_BYTES_Q4K
     if out is None:
-        out = np.empty((n_rows, nb * BLOCK_BYTES), dtype=np.uint8)
-    assert out.shape == (n_rows, nb * BLOCK_BYTES) and out.dtype == np.uint8 and out.flags.c_contiguous
+        out = np.empty((n_rows, nb * bb), dtype=np.uint8)
+    assert out.shape == (n_rows, nb * bb) and out.dtype == np.uint8 and out.flags.c_contiguous
     f = None
     if with_fields:
         f = Q5KFields(np.empty((n_rows, nb), np.uint16), np.empty((n_rows, nb), np.uint16),
                       np.empty((n_rows, nb, 8), np.uint8), np.empty((n_rows, nb, 8), np.uint8),
                       np.empty((n_rows, nb, 256), np.uint8))
-    rc = _load().synth_q5k_rows(
+    gen = _load().synth_q5k_rows if fmt == "q5_k" else _load().synth_q4k_rows
+    rc = gen(
         _ptr(out), row_begin, row_begin + n_rows, nb, key, D_RANGE[0], D_RANGE[1],
         DMIN_RANGE[0], DMIN_RANGE[1], float(d_mult),
         _ptr(f.d_bits if f else None), _ptr(f.dmin_bits if f else None),
@@ -143,14 +152,14 @@ def q5k_rows(n_rows: int, k: int, key: int, row_begin: int = 0, d_mult: float = 
 
 
 def q5k_matrix(n_rows: int, k: int, key: int, boost_rows=(), boost: float = 50.0,
-               with_fields: bool = False, out: np.ndarray | None = None):
-    """A whole Q5_K matrix; rows in boost_rows have d drawn x boost before fp16 rounding."""
-    res = q5k_rows(n_rows, k, key, 0, 1.0, with_fields, out)
+               with_fields: bool = False, out: np.ndarray | None = None, fmt: str = "q5_k"):
+    """A whole Q5_K (or Q4_K) matrix; rows in boost_rows have d drawn x boost before fp16 rounding."""
+    res = q5k_rows(n_rows, k, key, 0, 1.0, with_fields, out, fmt)
     w, f = (res if with_fields else (res, None))
     for r in boost_rows:
         if not 0 <= r < n_rows:
             continue
-        rr = q5k_rows(1, k, key, r, boost, with_fields)
+        rr = q5k_rows(1, k, key, r, boost, with_fields, None, fmt)
         if with_fields:
             w[r:r + 1], fr = rr
             f.d_bits[r], f.dmin_bits[r], f.sc[r], f.m[r], f.q[r] = fr.d_bits[0], fr.dmin_bits[0], fr.sc[0], fr.m[0], fr.q[0]

@@ -320,3 +320,75 @@ def test_log_softmax_sums_to_one_and_is_shift_invariant():
     assert np.allclose(lp2, lp, rtol=0, atol=1e-12) and np.allclose(lse2, lse + 13.0, rtol=0, atol=1e-12)
     # the order of the row is kept, and the argmax has the largest logprob
     assert np.array_equal(np.argmax(lp, axis=1), oracle.argmax_first(o))
+
+
+# ----------------------------------------------------------------- Q4_K (144-byte blocks)
+def _blank_q4k_block(d=1.0, dmin=0.5):
+    blk = np.zeros(144, np.uint8)
+    blk[:4] = _blank_block(d, dmin)[:4]
+    return blk
+
+
+def test_q4k_all_zero_quants_give_minus_dmin_times_min():
+    blk = _blank_q4k_block(d=0.00048828125, dmin=0.25)
+    for s in range(4):                                   # same scale-byte packing as Q5_K
+        blk[4 + 4 + s] = (s + 1) | (1 << 6)
+        blk[4 + 8 + s] = (s + 2) << 4
+    expect_m = [1, 2, 3, 4, 16 + 2, 16 + 3, 16 + 4, 16 + 5]
+    w = oracle.q4k_dequant_block(blk)
+    for e in range(256):
+        assert w[e] == -0.25 * expect_m[e // 32]
+
+
+def test_q4k_zero_scales_give_zero_and_max_gives_945_d():
+    blk = _blank_q4k_block(d=0.75, dmin=0.125)
+    blk[16:] = 0xA5
+    assert np.all(oracle.q4k_dequant_block(blk) == 0.0)
+    d = 0.000732421875
+    blk = _blank_q4k_block(d=d, dmin=0.0)
+    blk[4:8] = 0xFF
+    blk[12:16] = 0x0F
+    blk[16:] = 0xFF                                       # every nibble 15; there are no high bits
+    _, _, sc, m, q = oracle.q4k_parse(blk)
+    assert list(sc) == [63] * 8 and list(m) == [0] * 8 and np.all(q == 15)
+    assert np.all(oracle.q4k_dequant_block(blk) == 945.0 * d)
+
+
+@pytest.mark.parametrize("byte", [0, 5, 31, 32, 63, 64, 100, 127])
+def test_q4k_one_hot_nibbles_locate_their_weight(byte):
+    for nib in (0, 1):
+        blk = _blank_q4k_block()
+        blk[16 + byte] = 1 << (4 * nib)
+        _, _, _, _, q = oracle.q4k_parse(blk)
+        expect = np.zeros(256, np.int32)
+        expect[32 * (2 * (byte // 32) + nib) + byte % 32] = 1
+        assert np.array_equal(q, expect)
+
+
+def test_q4k_parse_recovers_every_generated_field():
+    w, f = synth.q5k_matrix(24, 1024, synth.stream_key(7, "pin-W4"), with_fields=True, fmt="q4_k")
+    assert w.shape == (24, 4 * 144) and f.q.max() <= 15
+    for i in range(24):
+        for kb in range(4):
+            d, dmin, sc, m, q = oracle.q4k_parse(w[i, kb * 144:(kb + 1) * 144])
+            assert d == float(f.d_bits[i, kb:kb + 1].view(np.float16)[0])
+            assert dmin == float(f.dmin_bits[i, kb:kb + 1].view(np.float16)[0])
+            assert np.array_equal(sc, f.sc[i, kb]) and np.array_equal(m, f.m[i, kb])
+            assert np.array_equal(q, f.q[i, kb])
+
+
+@pytest.mark.parametrize("n,k,b", [(1, 256, 1), (9, 512, 3), (40, 768, 2)])
+def test_q4k_matvec_brute_force_against_dense_numpy(n, k, b):
+    w, f = synth.q5k_matrix(n, k, synth.stream_key(n * 1000 + k, "pin-mv4"), with_fields=True, fmt="q4_k")
+    h = synth.normal_f64(b * k, synth.stream_key(b, "pin-mv4-h")).astype(np.float32).reshape(b, k)
+    out, raw = oracle.lmhead(h, None, w, 1.0, 0.0, want_raw=True, fmt="q4_k")
+    np.testing.assert_allclose(raw, h.astype(np.float64) @ _dense_from_fields(f).T, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(out, raw)
+    with pytest.raises(ValueError):                       # Q4_K bytes are not a Q5_K matrix of this K
+        oracle.lmhead(h, None, w, 1.0, 0.0)
+
+
+def test_q4k_head_byte_bill():
+    bill = {r[0]: int(r[1]) for r in read_golden("lmhead_byte_bill.txt")}
+    w = synth.q5k_matrix(2, 6656, synth.stream_key(0, "pin-bill4"), fmt="q4_k")
+    assert w.shape[1] * 202048 == bill["q4k_weight_bytes"]
