@@ -162,14 +162,14 @@ def _oracle_rate(wl, hidden, gamma, wq, target_s: float):
     cores = oracle.default_threads()
     probe = min(2048, wl.n_rows)
     t0 = time.perf_counter()
-    oracle.lmhead(hidden, gamma, wq[:probe], wl.scale, wl.cap, nthreads=cores)
+    oracle.lmhead(hidden, gamma, wq[:probe], wl.scale, wl.cap, nthreads=cores, fmt=wl.fmt)
     dt = max(time.perf_counter() - t0, 1e-6)
     rows = int(min(wl.n_rows, max(probe, probe * target_s / dt)))
     sample = np.ascontiguousarray(wq[:rows])
     reps = 0
     t0 = time.perf_counter()
     while True:                  # whole passes until the time budget is spent
-        oracle.lmhead(hidden, gamma, sample, wl.scale, wl.cap, nthreads=cores)
+        oracle.lmhead(hidden, gamma, sample, wl.scale, wl.cap, nthreads=cores, fmt=wl.fmt)
         reps += 1
         secs = time.perf_counter() - t0
         if secs >= target_s:
@@ -223,7 +223,7 @@ def _config(wl, ws, l2_mode):
                 "scale_cap": [[sc, cp] for (_, _, _, sc, cp) in wl.segments], "launches": 1, "l2": l2_mode,
                 "parallelism": f"replicas x{ws}"}
     return {"workload": wl.name, "n_rows": wl.n_rows, "k": wl.k, "batch": wl.batch,
-            "weights": "Q5_K 176 B / 256 weights", "final_norm": wl.norm, "scale": wl.scale, "cap": wl.cap,
+            "weights": "Q5_K 176 B / 256 weights" if wl.fmt == "q5_k" else "Q4_K 144 B / 256 weights", "final_norm": wl.norm, "scale": wl.scale, "cap": wl.cap,
             "argmax": wl.argmax, "l2": l2_mode, "parallelism": f"replicas x{ws}"}
 
 
@@ -390,7 +390,7 @@ def run_ours(args, wl):
     else:
         hidden, gamma, wq = synth.inputs_for(wl)
         w_d = torch.from_numpy(wq).to(dev)
-        head = mlh.LMHead(wl.n_rows, wl.k, max_batch=wl.batch, device=local)
+        head = mlh.LMHead(wl.n_rows, wl.k, max_batch=wl.batch, device=local, fmt=wl.fmt)
         logits = torch.empty((wl.batch, wl.n_rows), dtype=torch.float32, device=dev)
         amax = torch.empty((wl.batch,), dtype=torch.int32, device=dev) if wl.argmax else None
         path, launches = head.path_name(wl.batch), head.launches_per_forward(wl.batch, wl.norm)

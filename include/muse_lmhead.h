@@ -58,6 +58,10 @@ extern "C" {
 /* Largest batch a handle can be created for. */
 #define MUSE_MAX_BATCH 32
 
+/* Weight formats (muse_lmhead_init_format). */
+#define MUSE_FORMAT_Q5_K 0   /* 176-byte blocks: the LM head's format (Chapter 20 §20.3) */
+#define MUSE_FORMAT_Q4_K 1   /* 144-byte blocks: the FFN bulk's format, and the 756.5 MB head alternative of §20.8 */
+
 typedef struct muse_lmhead muse_lmhead;
 
 /*
@@ -70,6 +74,20 @@ typedef struct muse_lmhead muse_lmhead;
  */
 int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k,
                      int max_batch);
+
+/*
+ * The same for a matrix in another weight format: MUSE_FORMAT_Q5_K (what
+ * muse_lmhead_init uses) or MUSE_FORMAT_Q4_K, else MUSE_ERR_VALUE.  Q4_K is
+ * ggml's block_q4_K: fp16 d, fp16 dmin, the same 12 bytes of packed 6-bit
+ * scales and mins, then 128 bytes of nibbles placed as in Q5_K, no high bits
+ * (q in 0..15, w = d*sc*q - dmin*m); 144 bytes per 256 weights.  Every forward
+ * of the handle reads its weights in this format (weights = n_rows * (k/256) *
+ * 144 bytes for Q4_K).  Batch 1 with k = 4,096 or 6,656 runs the fused kernel;
+ * other shapes run the generic kernel (the tensor-core path reads Q5_K only).
+ * muse_lmhead_forward_group and muse_lmhead_forward_b1_noalloc read Q5_K only.
+ */
+int muse_lmhead_init_format(muse_lmhead **out, int device, int64_t n_rows, int64_t k,
+                            int max_batch, int format);
 
 /*
  * One forward on `stream` (a cudaStream_t; NULL = the legacy default stream),

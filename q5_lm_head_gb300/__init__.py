@@ -20,6 +20,7 @@ __all__ = [
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
     "muse_lmhead_forward_group", "MuseGemvSegment", "MUSE_MAX_SEGMENTS", "muse_lmhead_forward_logprobs",
+    "muse_lmhead_init_format", "MUSE_FORMAT_Q5_K", "MUSE_FORMAT_Q4_K", "BLOCK_BYTES",
     "EXPORTED_SYMBOLS",
     "LOGIT_SCALE", "SOFTCAP", "RMS_EPS",
 ]
@@ -38,12 +39,16 @@ EXPORTED_SYMBOLS = (
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
-    "muse_lmhead_forward_group", "muse_lmhead_forward_logprobs",
+    "muse_lmhead_forward_group", "muse_lmhead_forward_logprobs", "muse_lmhead_init_format",
 )
 
 MUSE_OK = 0
 MUSE_MAX_BATCH = 32
 MUSE_MAX_SEGMENTS = 4
+MUSE_FORMAT_Q5_K = 0
+MUSE_FORMAT_Q4_K = 1
+FORMATS = {"q5_k": MUSE_FORMAT_Q5_K, "q4_k": MUSE_FORMAT_Q4_K}
+BLOCK_BYTES = {"q5_k": 176, "q4_k": 144}
 STATUS_WAIT_TIMEOUT = 1
 
 _lib = None
@@ -78,6 +83,8 @@ def load_library():
     vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
     lib.muse_lmhead_init.restype = i32
     lib.muse_lmhead_init.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i32]
+    lib.muse_lmhead_init_format.restype = i32
+    lib.muse_lmhead_init_format.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i32, i32]
     lib.muse_lmhead_forward.restype = i32
     lib.muse_lmhead_forward.argtypes = [vp, vp, i32, vp, f32, vp, f32, f32, vp, vp, vp]
     lib.muse_lmhead_forward_host.restype = i32
@@ -109,6 +116,15 @@ def muse_lmhead_init(device: int, n_rows: int, k: int, max_batch: int) -> int:
     st = load_library().muse_lmhead_init(ctypes.byref(h), device, n_rows, k, max_batch)
     if st != MUSE_OK:
         raise MuseError(st, "muse_lmhead_init")
+    return h.value
+
+
+def muse_lmhead_init_format(device: int, n_rows: int, k: int, max_batch: int, fmt: int) -> int:
+    """Returns the handle (an integer) or raises MuseError."""
+    h = ctypes.c_void_p()
+    st = load_library().muse_lmhead_init_format(ctypes.byref(h), device, n_rows, k, max_batch, fmt)
+    if st != MUSE_OK:
+        raise MuseError(st, "muse_lmhead_init_format")
     return h.value
 
 
@@ -177,13 +193,17 @@ def muse_lmhead_forward_group(h: int | None, hidden: int, gamma: int | None, eps
 
 
 class LMHead:
-    """A handle for one [n_rows x k] Q5_K matrix and batches up to max_batch."""
+    """A handle for one [n_rows x k] Q5_K (or, fmt="q4_k", Q4_K) matrix and batches up to max_batch."""
 
-    def __init__(self, n_rows: int, k: int, max_batch: int = MUSE_MAX_BATCH, device: int | None = None):
+    def __init__(self, n_rows: int, k: int, max_batch: int = MUSE_MAX_BATCH, device: int | None = None,
+                 fmt: str = "q5_k"):
         import torch
+        if fmt not in FORMATS:
+            raise ValueError(f"fmt must be one of {sorted(FORMATS)}")
         self.device = torch.cuda.current_device() if device is None else int(device)
         self.n_rows, self.k, self.max_batch = int(n_rows), int(k), int(max_batch)
-        self.handle = muse_lmhead_init(self.device, self.n_rows, self.k, self.max_batch)
+        self.fmt, self.block_bytes = fmt, BLOCK_BYTES[fmt]
+        self.handle = muse_lmhead_init_format(self.device, self.n_rows, self.k, self.max_batch, FORMATS[fmt])
 
     def close(self):
         if getattr(self, "handle", None):
@@ -219,7 +239,7 @@ class LMHead:
         b = hidden.shape[0]
         hp = self._check(hidden, "hidden", torch.float32, (b, self.k))
         wp = self._check(weights, "weights", torch.uint8)
-        if weights.numel() != self.n_rows * (self.k // 256) * 176:
+        if weights.numel() != self.n_rows * (self.k // 256) * self.block_bytes:
             raise ValueError("weights: wrong number of bytes for this handle")
         gp = None if gamma is None else self._check(gamma, "gamma", torch.float32, (self.k,))
         if logits is None:
@@ -269,7 +289,7 @@ class LMHead:
         b = hidden.shape[0]
         hp = self._check(hidden, "hidden", torch.float32, (b, self.k))
         wp = self._check(weights, "weights", torch.uint8)
-        if weights.numel() != self.n_rows * (self.k // 256) * 176:
+        if weights.numel() != self.n_rows * (self.k // 256) * self.block_bytes:
             raise ValueError("weights: wrong number of bytes for this handle")
         gp = None if gamma is None else self._check(gamma, "gamma", torch.float32, (self.k,))
         if logprobs is None:
@@ -303,7 +323,7 @@ class LMHead:
         outs, descs = [], []
         for (w, n, scale, cap, out) in segments:
             wp = self._check(w, "weights", torch.uint8)
-            if w.numel() != n * (self.k // 256) * 176:
+            if w.numel() != n * (self.k // 256) * self.block_bytes:
                 raise ValueError("weights: wrong number of bytes for n_rows")
             if out is None:
                 out = torch.empty((n,), dtype=torch.float32, device=hidden.device)

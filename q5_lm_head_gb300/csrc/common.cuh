@@ -16,6 +16,10 @@ constexpr int kBlockWeights = 256;
 constexpr int kBlockBytes = 176;
 // byte offsets inside a Q5_K block
 constexpr int kOffD = 0, kOffDmin = 2, kOffScales = 4, kOffQh = 16, kOffQs = 48;
+// Q4_K block (144 bytes): the same d, dmin and scale bytes, then the nibbles
+// (no high bits); ggml's block_q4_K, the FFN bulk's format.
+constexpr int kBlockBytesQ4 = 144;
+constexpr int kOffQsQ4 = 16;
 
 // Scale then soft cap: v = raw * scale; cap > 0 ? cap * tanh(v / cap) : v.
 __device__ __forceinline__ float scale_softcap(float raw, float scale, float cap) {

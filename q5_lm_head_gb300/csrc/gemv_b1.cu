@@ -60,7 +60,8 @@ constexpr int kMaxSmem = 227 * 1024 - 1024;   // opt-in limit minus static share
 constexpr float kQuantMax = 4194300.0f;   // |xi| stays below 2^22 after rounding
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 
-template <int NB>
+// NB blocks per row; kQ4: Q4_K blocks (144 bytes, nibbles only) instead of Q5_K.
+template <int NB, bool kQ4>
 struct B1Cfg {
   static constexpr int kUnits = 4 * NB;                    // (block, 64-column group) units per row
   static constexpr int kConsumers = kUnits * kStreams;
@@ -70,7 +71,8 @@ struct B1Cfg {
   static constexpr int kConsumerWarps = kConsumers / 32;
   static constexpr int kProducerWarps = 2;
   static constexpr int kThreads = kConsumers + 32 * kProducerWarps;
-  static constexpr int kRowBytes = NB * kBlockBytes;
+  static constexpr int kBB = kQ4 ? kBlockBytesQ4 : kBlockBytes;   // bytes per block
+  static constexpr int kRowBytes = NB * kBB;
   static constexpr int kStageBytes = kRows * kRowBytes;
   static constexpr int kSlotBytes = kRows * NB * 4;         // one partial per (row, block)
   static constexpr int kFixedBytes = 512;                   // barriers + scratch
@@ -80,7 +82,10 @@ struct B1Cfg {
   static constexpr int kSlots = kStages + 2;
   static constexpr int kSmemBytes = kStages * kStageBytes + kSlots * kSlotBytes + kFixedBytes;
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
-  static_assert(2 * NB * kBlockWeights * 4 <= kStageBytes, "hidden + gamma fit one stage");
+  // the prologue stages hidden (and gamma) in the last stage, or gamma in the one
+  // before when both do not fit one stage
+  static_assert(NB * kBlockWeights * 4 <= kStageBytes, "hidden fits one stage");
+  static constexpr int kHoldStages = 2 * NB * kBlockWeights * 4 <= kStageBytes ? 1 : 2;
   // after the activations are loaded the staging stage holds, per unit, the
   // four (amax, sum) pairs of its quarters and its plane words (p2, p1, p0:
   // 16 words each, padded to 52 so the units' rows fall on distinct banks)
@@ -126,6 +131,7 @@ struct UnitSel {
   int qs_off;          // byte offset of this thread's 32 low-nibble bytes
 };
 
+template <bool kQ4>
 __device__ __forceinline__ UnitSel make_unit_sel(int c) {
   UnitSel u;
   u.upper = c >= 2;
@@ -135,28 +141,40 @@ __device__ __forceinline__ UnitSel make_unit_sel(int c) {
   u.sh_hi2 = u.upper ? 16u * (c - 2) + 2u : 0u;
   u.msk_hi = u.upper ? 0x3030u : 0u;
   u.rot = static_cast<uint32_t>(4 - 2 * c) & 31u;
-  u.qs_off = kOffQs + 32 * c;
+  u.qs_off = (kQ4 ? kOffQsQ4 : kOffQs) + 32 * c;
   return u;
 }
 
 // This thread's contribution to one row: sum over its 64 columns of
-// (d*sc_s*q - dmin*m_s) * x, from the row's Q5_K block `blk` in shared memory.
+// (d*sc_s*q - dmin*m_s) * x, from the row's Q5_K (or Q4_K) block `blk` in
+// shared memory.
+template <bool kQ4>
 __device__ __forceinline__ float unit_partial(const uint8_t *blk, const UnitSel &us, const XPlanes &xl,
                                               const XPlanes &xh, float sx_lo, float sx_hi, float sigma_half) {
   const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-  const uint4 qh0 = *reinterpret_cast<const uint4 *>(blk + kOffQh);
-  const uint4 qh1 = *reinterpret_cast<const uint4 *>(blk + kOffQh + 16);
   const uint4 qs0 = *reinterpret_cast<const uint4 *>(blk + us.qs_off);
   const uint4 qs1 = *reinterpret_cast<const uint4 *>(blk + us.qs_off + 16);
-  const uint32_t H[8] = {qh0.x, qh0.y, qh0.z, qh0.w, qh1.x, qh1.y, qh1.z, qh1.w};
   const uint32_t A[8] = {qs0.x, qs0.y, qs0.z, qs0.w, qs1.x, qs1.y, qs1.z, qs1.w};
+  uint32_t H[8] = {};
+  if constexpr (!kQ4) {
+    const uint4 qh0 = *reinterpret_cast<const uint4 *>(blk + kOffQh);
+    const uint4 qh1 = *reinterpret_cast<const uint4 *>(blk + kOffQh + 16);
+    H[0] = qh0.x; H[1] = qh0.y; H[2] = qh0.z; H[3] = qh0.w;
+    H[4] = qh1.x; H[5] = qh1.y; H[6] = qh1.z; H[7] = qh1.w;
+  }
   int l2 = 0, h2 = 0;
   unsigned l1 = 0, l0 = 0, h1 = 0, h0 = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t t = rotl32(H[i], us.rot);                             // high bits at 4 (lo) and 5 (hi)
-    const uint32_t qlo = (A[i] & 0x0F0F0F0Fu) | (t & 0x10101010u);       // q
-    const uint32_t qhi = ((A[i] >> 3) & 0x1E1E1E1Eu) | (t & 0x20202020u);  // 2q
+    uint32_t qlo, qhi;
+    if constexpr (kQ4) {
+      qlo = A[i] & 0x0F0F0F0Fu;                                          // q
+      qhi = (A[i] >> 3) & 0x1E1E1E1Eu;                                   // 2q
+    } else {
+      const uint32_t t = rotl32(H[i], us.rot);                           // high bits at 4 (lo) and 5 (hi)
+      qlo = (A[i] & 0x0F0F0F0Fu) | (t & 0x10101010u);                    // q
+      qhi = ((A[i] >> 3) & 0x1E1E1E1Eu) | (t & 0x20202020u);             // 2q
+    }
     l2 = __dp4a(static_cast<int>(qlo), static_cast<int>(xl.p2[i]), l2);
     l1 = __dp4a(qlo, xl.p1[i], l1);
     l0 = __dp4a(qlo, xl.p0[i], l0);
@@ -214,12 +232,12 @@ __device__ __forceinline__ TileLoc locate(const SegTable &T, int64_t tile) {
   return L;
 }
 
-template <int NB, bool kGroup>
-__global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
+template <int NB, bool kGroup, bool kQ4>
+__global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     gemv_b1_kernel(const float *__restrict__ hidden, const float *__restrict__ gamma, float eps,
                    const __grid_constant__ SegTable segs, unsigned long long *keys, unsigned int *ticket,
                    int32_t *argmax, uint32_t *status, float2 *lse_parts) {
-  using C = B1Cfg<NB>;
+  using C = B1Cfg<NB, kQ4>;
   constexpr int K = NB * kBlockWeights;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *stages = smem;
@@ -229,9 +247,12 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
   uint64_t *pro_full = empty + C::kStages;                                 // hidden (+ gamma) staged
   uint64_t *pro_done = pro_full + 1;                                       // consumers done with them
   float *s_red = reinterpret_cast<float *>(pro_done + 1);                  // [32]
-  // the prologue's staging area: the last stage, until its first weight tile
+  // the prologue's staging area: the last stage (and the one before, for gamma,
+  // when both rows do not fit one stage), until their first weight tiles
   const float *s_hidden = reinterpret_cast<const float *>(stages + (C::kStages - 1) * C::kStageBytes);
-  const float *s_gamma = s_hidden + K;
+  const float *s_gamma = C::kHoldStages == 1
+                             ? s_hidden + K
+                             : reinterpret_cast<const float *>(stages + (C::kStages - 2) * C::kStageBytes);
   unsigned long long *s_best = reinterpret_cast<unsigned long long *>(s_red + 32);
   volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(s_best + 1);
   float2 *s_ms = reinterpret_cast<float2 *>(s_best + 2);                   // [2] producers' (max, sum exp)
@@ -267,10 +288,9 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
     constexpr int kHoldTile = C::kStages - 1;  // local tile whose stage holds the prologue data
     if (pw == (kHoldTile & 1) && lane == 0) {
       const uint32_t row_bytes = static_cast<uint32_t>(K) * 4u;
-      uint8_t *dst = stages + kHoldTile * C::kStageBytes;
       ptx::mbar_arrive_expect_tx(pro_full, gamma ? 2u * row_bytes : row_bytes);
-      ptx::bulk_g2s_nohint(dst, hidden, row_bytes, pro_full);
-      if (gamma) ptx::bulk_g2s_nohint(dst + row_bytes, gamma, row_bytes, pro_full);
+      ptx::bulk_g2s_nohint(const_cast<float *>(s_hidden), hidden, row_bytes, pro_full);
+      if (gamma) ptx::bulk_g2s_nohint(const_cast<float *>(s_gamma), gamma, row_bytes, pro_full);
     }
     // epilogue: lane pair (2er, 2er+1) sums row er's block partials, alternating
     static_assert(kRows <= 16, "two lanes per row");
@@ -316,7 +336,7 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
         aborted = true;
         break;
       }
-      if (j == kHoldTile) {                    // the consumers still read the prologue data there
+      if (j == kHoldTile || (C::kHoldStages == 2 && j == kHoldTile - 1)) {   // prologue data still there
         bool ok = true;
         if (lane == 0) ok = ptx::mbar_wait(pro_done, 0);
         if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) {
@@ -458,7 +478,7 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(pro_done);
     }
-    const UnitSel us = make_unit_sel(c);
+    const UnitSel us = make_unit_sel<kQ4>(c);
 
     int st = 0, ps = 0;
     uint32_t ph = 0;                           // round parity of the stage ring
@@ -471,18 +491,18 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
       }
       const int rows = locate<kGroup>(segs, tile).rows;
       float *slot = slots + ps * (C::kSlotBytes / 4) + kb;
-      const uint8_t *sbase = stages + st * C::kStageBytes + kb * kBlockBytes;
+      const uint8_t *sbase = stages + st * C::kStageBytes + kb * C::kBB;
       float pv[kRows / kStreams];
       if (rows == kRows) {
 #pragma unroll
         for (int rr = 0; rr < kRows / kStreams; ++rr)
-          pv[rr] = unit_partial(sbase + (stream + rr * kStreams) * C::kRowBytes, us, xl, xh, sx_lo, sx_hi,
+          pv[rr] = unit_partial<kQ4>(sbase + (stream + rr * kStreams) * C::kRowBytes, us, xl, xh, sx_lo, sx_hi,
                                 sigma_half);
       } else {
 #pragma unroll
         for (int rr = 0; rr < kRows / kStreams; ++rr) {
           const int rl = stream + rr * kStreams;
-          pv[rr] = rl < rows ? unit_partial(sbase + rl * C::kRowBytes, us, xl, xh, sx_lo, sx_hi, sigma_half)
+          pv[rr] = rl < rows ? unit_partial<kQ4>(sbase + rl * C::kRowBytes, us, xl, xh, sx_lo, sx_hi, sigma_half)
                              : 0.0f;
         }
       }
@@ -508,25 +528,25 @@ __global__ void __launch_bounds__(B1Cfg<NB>::kThreads, 1)
   if (argmax) argmax_publish_finish(keys, ticket, argmax, s_best, 1);
 }
 
-template <int NB, bool kGroup>
+template <int NB, bool kGroup, bool kQ4>
 cudaError_t launch_b1_nb(const float *hidden, const float *gamma, float eps, const SegTable &T,
                          unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status,
                          float2 *lse_parts, int num_sms, cudaStream_t stream) {
-  using C = B1Cfg<NB>;
+  using C = B1Cfg<NB, kQ4>;
   static unsigned long long configured = 0;   // one bit per device: the attribute is per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured & bit)) {
-    e = cudaFuncSetAttribute(gemv_b1_kernel<NB, kGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gemv_b1_kernel<NB, kGroup, kQ4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
   const int64_t n_tiles = T.tile_end[T.n - 1];
   const int64_t grid = n_tiles < num_sms ? n_tiles : num_sms;
-  gemv_b1_kernel<NB, kGroup><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
+  gemv_b1_kernel<NB, kGroup, kQ4><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
       hidden, gamma, eps, T, keys, ticket, argmax, status, lse_parts);
   return cudaGetLastError();
 }
@@ -556,11 +576,19 @@ cudaError_t launch_b1(const LaunchArgs &a) {
   const GemvSegment one = {a.w, a.logits, a.n_rows, a.scale, a.cap};
   const SegTable T = make_table(&one, 1);
   float2 *parts = a.lse_parts ? a.ws.lse_parts : nullptr;   // batch row 0: one pair per CTA
-  switch (a.k / kBlockWeights) {
-    case 26: return launch_b1_nb<26, false>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
-                                            a.ws.status, parts, a.num_sms, a.stream);
-    case 16: return launch_b1_nb<16, false>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
-                                            a.ws.status, parts, a.num_sms, a.stream);
+  const int nb = a.k / kBlockWeights;
+  if (a.q4) {
+    if (nb == 26) return launch_b1_nb<26, false, true>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket,
+                                                       a.argmax, a.ws.status, parts, a.num_sms, a.stream);
+    if (nb == 16) return launch_b1_nb<16, false, true>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket,
+                                                       a.argmax, a.ws.status, parts, a.num_sms, a.stream);
+    return cudaErrorInvalidValue;
+  }
+  switch (nb) {
+    case 26: return launch_b1_nb<26, false, false>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
+                                                   a.ws.status, parts, a.num_sms, a.stream);
+    case 16: return launch_b1_nb<16, false, false>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
+                                                   a.ws.status, parts, a.num_sms, a.stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -570,10 +598,10 @@ cudaError_t launch_b1_group(const float *hidden, const float *gamma, float eps, 
   if (n < 1 || n > kMaxSegments) return cudaErrorInvalidValue;
   const SegTable T = make_table(segs, n);
   switch (k / kBlockWeights) {
-    case 26: return launch_b1_nb<26, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status, nullptr,
-                                           num_sms, stream);
-    case 16: return launch_b1_nb<16, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status, nullptr,
-                                           num_sms, stream);
+    case 26: return launch_b1_nb<26, true, false>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status,
+                                                  nullptr, num_sms, stream);
+    case 16: return launch_b1_nb<16, true, false>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status,
+                                                  nullptr, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -4,7 +4,7 @@
 //            the handle's x buffer ("Chapter 20 — Final norm, LM head, and the
 //            soft cap" §20.1: x = h / sqrt(mean(h^2) + eps) * gamma)
 //   launch 2: one warp per weight row; every lane dequantises 8 weights of each
-//            Q5_K block (w = d*sc*q - dmin*m, §20.3 block) straight from global
+//            Q5_K (or Q4_K) block (w = d*sc*q - dmin*m, §20.3 block) straight from global
 //            memory, multiplies them with x (read through L1), warp-shuffle
 //            reduction, scale + soft cap epilogue (§20.4), and the two-level argmax
 //            (per-CTA shared-memory max, then one global atomic per CTA and row).
@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kNormThreads)
 constexpr int kGemvThreads = 256;
 constexpr int kBatchTile = 4;
 
+template <bool kQ4>
 __global__ void __launch_bounds__(kGemvThreads)
     gemv_generic_kernel(const uint8_t *__restrict__ w, const float *__restrict__ x, int batch,
                         int64_t n_rows, int k, float scale, float cap, float *__restrict__ logits,
@@ -70,16 +71,17 @@ __global__ void __launch_bounds__(kGemvThreads)
   const int64_t warps_per_cta = kGemvThreads / 32;
   const int64_t n_warps = static_cast<int64_t>(gridDim.x) * warps_per_cta;
   for (int64_t row = blockIdx.x * warps_per_cta + (threadIdx.x >> 5); row < n_rows; row += n_warps) {
-    const uint8_t *wrow = w + row * nb * kBlockBytes;
+    constexpr int kBB = kQ4 ? kBlockBytesQ4 : kBlockBytes;
+    const uint8_t *wrow = w + row * nb * kBB;
     for (int b0 = 0; b0 < batch; b0 += kBatchTile) {
       float acc[kBatchTile];
 #pragma unroll
       for (int t = 0; t < kBatchTile; ++t) acc[t] = 0.0f;
       for (int kb = 0; kb < nb; ++kb) {
-        const uint8_t *blk = wrow + kb * kBlockBytes;
+        const uint8_t *blk = wrow + kb * kBB;
         const uint4 hdr = __ldg(reinterpret_cast<const uint4 *>(blk));
-        const uint32_t qh = __ldg(reinterpret_cast<const uint32_t *>(blk + kOffQh) + j4);
-        const uint32_t qs = __ldg(reinterpret_cast<const uint32_t *>(blk + kOffQs + 32 * c) + j4);
+        const uint32_t qh = kQ4 ? 0u : __ldg(reinterpret_cast<const uint32_t *>(blk + kOffQh) + j4);
+        const uint32_t qs = __ldg(reinterpret_cast<const uint32_t *>(blk + (kQ4 ? kOffQsQ4 : kOffQs) + 32 * c) + j4);
         const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
         const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
         int sc0, m0, sc1, m1;
@@ -150,8 +152,12 @@ cudaError_t launch_generic(const LaunchArgs &a) {
   int64_t blocks = (warps_needed + (kGemvThreads / 32) - 1) / (kGemvThreads / 32);
   const int64_t cap_blocks = static_cast<int64_t>(a.num_sms) * 8;
   if (blocks > cap_blocks) blocks = cap_blocks;
-  gemv_generic_kernel<<<static_cast<unsigned>(blocks), kGemvThreads, 0, a.stream>>>(
-      a.w, x, a.batch, a.n_rows, a.k, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax);
+  if (a.q4)
+    gemv_generic_kernel<true><<<static_cast<unsigned>(blocks), kGemvThreads, 0, a.stream>>>(
+        a.w, x, a.batch, a.n_rows, a.k, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax);
+  else
+    gemv_generic_kernel<false><<<static_cast<unsigned>(blocks), kGemvThreads, 0, a.stream>>>(
+        a.w, x, a.batch, a.n_rows, a.k, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,7 @@
 
 struct muse_lmhead {
   int device;
+  int format;              // MUSE_FORMAT_Q5_K or MUSE_FORMAT_Q4_K
   int64_t n_rows;
   int64_t k;
   int max_batch;
@@ -58,7 +59,7 @@ enum class Path { B1, TensorCore, Generic };
 
 Path choose_path(const muse_lmhead *h, int batch) {
   if (batch == 1 && muse::b1_supported(static_cast<int>(h->k))) return Path::B1;
-  if (muse::tc_supported(batch, static_cast<int>(h->k))) return Path::TensorCore;
+  if (h->format == MUSE_FORMAT_Q5_K && muse::tc_supported(batch, static_cast<int>(h->k))) return Path::TensorCore;
   return Path::Generic;
 }
 
@@ -93,6 +94,7 @@ int run_forward(muse_lmhead *h, const float *hidden, int batch, const float *gam
   a.ws = h->ws;
   a.stream = stream;
   a.lse_parts = lse_parts;
+  a.q4 = h->format == MUSE_FORMAT_Q4_K;
   cudaError_t e;
   switch (choose_path(h, batch)) {
     case Path::B1: e = muse::launch_b1(a); break;
@@ -114,8 +116,14 @@ int run_forward(muse_lmhead *h, const float *hidden, int batch, const float *gam
 extern "C" {
 
 int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k, int max_batch) {
+  return muse_lmhead_init_format(out, device, n_rows, k, max_batch, MUSE_FORMAT_Q5_K);
+}
+
+int muse_lmhead_init_format(muse_lmhead **out, int device, int64_t n_rows, int64_t k, int max_batch,
+                            int format) {
   if (!out) return MUSE_ERR_NULL;
   *out = nullptr;
+  if (format != MUSE_FORMAT_Q5_K && format != MUSE_FORMAT_Q4_K) return MUSE_ERR_VALUE;
   if (n_rows < 1 || n_rows > (int64_t{1} << 31) - 1 || k < 256 || k % 256 != 0 || k > (1 << 20))
     return MUSE_ERR_SHAPE;
   if (max_batch < 1 || max_batch > MUSE_MAX_BATCH) return MUSE_ERR_BATCH;
@@ -133,6 +141,7 @@ int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k, i
   muse_lmhead *h = new (std::nothrow) muse_lmhead();
   if (!h) return MUSE_ERR_NOMEM;
   h->device = device;
+  h->format = format;
   h->n_rows = n_rows;
   h->k = k;
   h->max_batch = max_batch;
@@ -174,6 +183,7 @@ int muse_lmhead_forward_group(muse_lmhead *h, const float *hidden, const float *
   if (!h || !hidden || !segments) return MUSE_ERR_NULL;
   if (n_segments < 1 || n_segments > MUSE_MAX_SEGMENTS) return MUSE_ERR_SHAPE;
   if (!muse::b1_supported(static_cast<int>(h->k))) return MUSE_ERR_SHAPE;
+  if (h->format != MUSE_FORMAT_Q5_K) return MUSE_ERR_VALUE;   // the grouped kernel reads Q5_K
   if (gamma && (!std::isfinite(eps) || eps < 0.0f)) return MUSE_ERR_VALUE;
   if (!aligned(hidden, 16) || (gamma && !aligned(gamma, 16))) return MUSE_ERR_ALIGN;
   muse::GemvSegment segs[muse::kMaxSegments];

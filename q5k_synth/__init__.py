@@ -206,11 +206,16 @@ class Workload:
     row_scale: tuple | None = None   # (lo, hi): hidden row b multiplied by U(lo, hi)
     hidden_tag: str = ""
     gamma_tag: str = "G:lmhead"
+    fmt: str = "q5_k"                  # weight blocks: q5_k (176 bytes) or q4_k (144 bytes)
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
     @property
+    def block_bytes(self) -> int:
+        return BLOCK_BYTES if self.fmt == "q5_k" else BLOCK_BYTES_Q4K
+
+    @property
     def weight_bytes(self) -> int:
-        return self.n_rows * (self.k // BLOCK_WEIGHTS) * BLOCK_BYTES
+        return self.n_rows * (self.k // BLOCK_WEIGHTS) * self.block_bytes
 
     def algorithmic_bytes(self) -> int:
         """Q5_K weights + hidden + gamma + logits: the bytes one forward must move."""
@@ -240,6 +245,9 @@ WORKLOADS: dict[str, Workload] = {
 }
 for _b in (1, 2, 4, 8, 16, 32):
     WORKLOADS[f"sweep_b{_b}"] = _lm(f"sweep_b{_b}", _b)
+# the Q4_K head alternative (756.5 MB), batch 1, same shapes and boosted rows
+WORKLOADS["lmhead_q4k_b1"] = Workload("lmhead_q4k_b1", VOCAB, HIDDEN, 1, "W:lmhead_q4k", boost_rows=BOOSTED_ROWS,
+                                      hidden_tag="H:lmhead_q4k_b1", fmt="q4_k")
 
 
 @dataclass(frozen=True)
@@ -310,7 +318,7 @@ def gamma_for(w: Workload, seed: int = 0) -> np.ndarray | None:
 
 def weights_for(w: Workload, seed: int = 0, with_fields: bool = False, out=None):
     return q5k_matrix(w.n_rows, w.k, stream_key(seed, w.weight_tag), w.boost_rows, 50.0,
-                      with_fields, out)
+                      with_fields, out, w.fmt)
 
 
 def inputs_for(w: Workload | str, seed: int = 0, with_fields: bool = False):

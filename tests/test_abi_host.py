@@ -63,6 +63,8 @@ def test_validation_fails_closed_without_cuda(lib):
     assert lib.muse_lmhead_init(ctypes.byref(h), 0, 10, 0, 1) == -2
     assert lib.muse_lmhead_init(ctypes.byref(h), 0, 10, 256, 0) == -3     # max_batch
     assert lib.muse_lmhead_init(ctypes.byref(h), 0, 10, 256, 33) == -3
+    assert lib.muse_lmhead_init_format(ctypes.byref(h), 0, 10, 256, 1, 2) == -5   # unknown weight format
+    assert lib.muse_lmhead_init_format(None, 0, 10, 256, 1, 1) == -1
     assert h.value is None
     assert lib.muse_lmhead_forward(None, 16, 1, None, 1e-5, 16, 1.0, 0.0, 16, None, None) == -1
     assert lib.muse_lmhead_forward_host(None, 16, 1, None, 1e-5, 16, 1.0, 0.0, 16, None, None) == -1

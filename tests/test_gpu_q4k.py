@@ -1,0 +1,117 @@
+"""GPU parity of Q4_K weights (144-byte blocks: ggml's block_q4_K, the FFN
+bulk's format and the 756.5 MB alternative head of "Chapter 20 — Final norm,
+LM head, and the soft cap" §20.8) against the f64 oracle's own Q4_K parser.
+
+Same bar as Q5_K: |gpu - oracle| <= 2e-3 on every logit, argmax equal where
+the oracle's top-2 gap exceeds 4e-3.  Covers the fused batch-1 kernel (K =
+6,656 and 4,096), the generic kernel (batches > 1, other K) and the logprobs
+forward.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import q5k_synth as synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+GAP = 4e-3
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    import q5_lm_head_gb300 as mlh
+    from q5_lm_head_gb300 import _build
+    _build.build()
+    mlh.load_library()
+    torch.cuda.set_device(0)
+    return torch
+
+
+def _dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
+
+
+def _check(got, am, ref):
+    err = np.abs(got.astype(np.float64) - ref)
+    assert err.max() <= TOL, f"max|err|={err.max():.3g}"
+    if am is not None:
+        gap, want = oracle.top2_gap(ref), oracle.argmax_first(ref)
+        for b in range(ref.shape[0]):
+            assert am[b] == int(np.argmax(got[b]))
+            if gap[b] > GAP:
+                assert am[b] == want[b]
+
+
+def _run(torch, hidden, gamma, wq, n, k, scale, cap, path=None, want_argmax=True):
+    import q5_lm_head_gb300 as mlh
+    b = hidden.shape[0]
+    with mlh.LMHead(n, k, max_batch=b, device=0, fmt="q4_k") as head:
+        if path is not None:
+            assert head.path_name(b) == path
+        out = head.forward(_dev(torch, hidden), _dev(torch, wq), None if gamma is None else _dev(torch, gamma),
+                           synth.RMS_EPS, scale, cap, want_argmax)
+        torch.cuda.synchronize()
+        assert head.device_status() == 0
+    if want_argmax:
+        return out[0].cpu().numpy(), out[1].cpu().numpy()
+    return out.cpu().numpy(), None
+
+
+def test_q4k_full_head_batch1(torch_cuda):
+    wl = synth.WORKLOADS["lmhead_q4k_b1"]
+    hidden, gamma, wq = synth.inputs_for(wl)
+    assert wq.shape == (wl.n_rows, 26 * 144)
+    got, am = _run(torch_cuda, hidden, gamma, wq, wl.n_rows, wl.k, wl.scale, wl.cap, "gemv_b1")
+    _check(got, am, oracle.lmhead(hidden, gamma, wq, wl.scale, wl.cap, synth.RMS_EPS, fmt="q4_k"))
+
+
+@pytest.mark.parametrize("n,k,b,norm,cap", [
+    (777, 4096, 1, True, 20.0),     # fused kernel, K = 4,096
+    (25, 6656, 1, False, 0.0),      # fewer rows than one stage per CTA
+    (3001, 6656, 3, True, 20.0),    # generic kernel (the tensor-core path reads Q5_K only)
+    (500, 512, 1, True, 20.0),      # generic kernel, K with no fused kernel
+    (64, 768, 8, False, 0.0),
+])
+def test_q4k_shapes(torch_cuda, n, k, b, norm, cap):
+    rng = np.random.default_rng(n * 7 + k + b)
+    hidden = rng.standard_normal((b, k)).astype(np.float32)
+    gamma = (1.0 + 0.1 * rng.standard_normal(k)).astype(np.float32) if norm else None
+    wq = synth.q5k_matrix(n, k, synth.stream_key(9, f"W:q4:{n}:{k}"), boost_rows=(n // 2,), boost=50.0,
+                          fmt="q4_k")
+    scale = synth.LOGIT_SCALE if cap > 0 else 1.0
+    got, am = _run(torch_cuda, hidden, gamma, wq, n, k, scale, cap)
+    _check(got, am, oracle.lmhead(hidden, gamma, wq, scale, cap, synth.RMS_EPS, fmt="q4_k"))
+
+
+def test_q4k_logprobs_batch1(torch_cuda):
+    import q5_lm_head_gb300 as mlh
+    torch = torch_cuda
+    n, k = 30000, 6656
+    rng = np.random.default_rng(5)
+    hidden = rng.standard_normal((1, k)).astype(np.float32)
+    gamma = (1.0 + 0.1 * rng.standard_normal(k)).astype(np.float32)
+    wq = synth.q5k_matrix(n, k, synth.stream_key(10, "W:q4lp"), fmt="q4_k")
+    with mlh.LMHead(n, k, max_batch=1, device=0, fmt="q4_k") as head:
+        lp, lse, am = head.forward_logprobs(_dev(torch, hidden), _dev(torch, wq), _dev(torch, gamma))
+        torch.cuda.synchronize()
+        lp, lse = lp.cpu().numpy(), lse.cpu().numpy()
+    ref_lp, ref_lse = oracle.log_softmax(oracle.lmhead(hidden, gamma, wq, synth.LOGIT_SCALE, synth.SOFTCAP,
+                                                       synth.RMS_EPS, fmt="q4_k"))
+    assert np.abs(lp - ref_lp).max() <= TOL and np.abs(lse - ref_lse).max() <= TOL
+
+
+def test_q4k_handle_rejects_q5k_sized_weights_and_the_group_call(torch_cuda):
+    import q5_lm_head_gb300 as mlh
+    torch = torch_cuda
+    n, k = 64, 6656
+    w5 = _dev(torch, synth.q5k_matrix(n, k, synth.stream_key(0, "W:q4-wrong")))
+    with mlh.LMHead(n, k, max_batch=1, device=0, fmt="q4_k") as head:
+        with pytest.raises(ValueError):
+            head.forward(torch.zeros((1, k), device="cuda"), w5)
+        out = torch.empty((n,), dtype=torch.float32, device="cuda")
+        st = mlh.muse_lmhead_forward_group(head.handle, torch.zeros((k,), device="cuda").data_ptr(), None, 1e-5,
+                                           [(w5.data_ptr(), n, out.data_ptr(), 1.0, 0.0)], None)
+        assert st == -5                                   # the grouped kernel reads Q5_K only
