@@ -104,7 +104,8 @@ class ClockSampler:
 
 # ncu summaries that carry a per-launch DRAM traffic figure: (file, workload, kernel sources)
 _PROFILED = {"gemv_b1": ("gemv_b1_lmhead.md", "lmhead_b1", ("gemv_b1.cu", "common.cuh", "ptx.cuh")),
-             "gemm_tc": ("gemm_tc_lmhead_b8.md", "lmhead_b8", ("gemm_tc.cu", "common.cuh", "ptx.cuh", "tc.cuh"))}
+             "gemm_tc": ("gemm_tc_lmhead_b8.md", "lmhead_b8", ("gemm_tc.cu", "common.cuh", "ptx.cuh", "tc.cuh")),
+             "gemv_b1_group": ("gemv_b1_group_attn_qkvg.md", "attn_qkvg", ("gemv_b1.cu", "common.cuh", "ptx.cuh"))}
 
 
 def _profiled_traffic(kernel_path: str, workload: str):
