@@ -163,6 +163,23 @@ const char *muse_lmhead_path_name(const muse_lmhead *h, int batch);
 int muse_lmhead_device_status(muse_lmhead *h, uint32_t *status_out);
 
 /*
+ * Clear the handle's status word (asynchronous 4-byte memset on `stream`), for
+ * example after a recorded timeout, once the caller has dealt with it.
+ */
+int muse_lmhead_clear_device_status(muse_lmhead *h, void *stream);
+
+/*
+ * Self-test of the failure path the pipelined kernels rely on: launches a
+ * one-thread kernel on `stream` that waits on an mbarrier nothing ever arrives
+ * on.  The wait is bounded like every wait in the library (at most 2^16 polls,
+ * each suspended for at most 20 us); it gives up, sets bit 0 of the handle's
+ * status word and the kernel returns normally — no trap, no fault, the context
+ * stays usable.  Read the result with muse_lmhead_device_status and clear it
+ * with muse_lmhead_clear_device_status.  The pages have no counterpart.
+ */
+int muse_lmhead_selftest_wait_timeout(muse_lmhead *h, void *stream);
+
+/*
  * Batch-1 forward for callers that cannot allocate device memory at call time
  * (code running during CUDA graph capture, runtimes that reserve all device
  * memory through their own allocator, serving loops that must not risk the

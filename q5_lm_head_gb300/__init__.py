@@ -21,6 +21,7 @@ __all__ = [
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
     "muse_lmhead_forward_group", "MuseGemvSegment", "MUSE_MAX_SEGMENTS", "muse_lmhead_forward_logprobs",
     "muse_lmhead_init_format", "MUSE_FORMAT_Q5_K", "MUSE_FORMAT_Q4_K", "BLOCK_BYTES",
+    "muse_lmhead_clear_device_status", "muse_lmhead_selftest_wait_timeout",
     "EXPORTED_SYMBOLS",
     "LOGIT_SCALE", "SOFTCAP", "RMS_EPS",
 ]
@@ -40,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
     "muse_lmhead_forward_group", "muse_lmhead_forward_logprobs", "muse_lmhead_init_format",
+    "muse_lmhead_clear_device_status", "muse_lmhead_selftest_wait_timeout",
 )
 
 MUSE_OK = 0
@@ -101,6 +103,10 @@ def load_library():
     lib.muse_lmhead_status_string.argtypes = [i32]
     lib.muse_lmhead_forward_b1_noalloc.restype = i32
     lib.muse_lmhead_forward_b1_noalloc.argtypes = [i32, vp, vp, f32, vp, i64, i64, f32, f32, vp, vp, vp]
+    lib.muse_lmhead_clear_device_status.restype = i32
+    lib.muse_lmhead_clear_device_status.argtypes = [vp, vp]
+    lib.muse_lmhead_selftest_wait_timeout.restype = i32
+    lib.muse_lmhead_selftest_wait_timeout.argtypes = [vp, vp]
     lib.muse_lmhead_forward_logprobs.restype = i32
     lib.muse_lmhead_forward_logprobs.argtypes = [vp, vp, i32, vp, f32, vp, f32, f32, vp, vp, vp, vp]
     lib.muse_lmhead_forward_group.restype = i32
@@ -176,6 +182,14 @@ def muse_lmhead_status_string(status: int) -> str:
 
 
 # ------------------------------------------------------------ torch-facing wrapper
+def muse_lmhead_clear_device_status(h: int, stream: int | None = None) -> int:
+    return load_library().muse_lmhead_clear_device_status(h, stream)
+
+
+def muse_lmhead_selftest_wait_timeout(h: int, stream: int | None = None) -> int:
+    return load_library().muse_lmhead_selftest_wait_timeout(h, stream)
+
+
 def muse_lmhead_forward_logprobs(h: int, hidden: int, batch: int, gamma: int | None, eps: float, weights: int,
                                  scale: float, cap: float, logprobs: int, lse: int | None, argmax: int | None,
                                  stream: int | None) -> int:

@@ -70,6 +70,10 @@ cudaError_t launch_logprob_apply(float *logits, int batch, int64_t n_rows, const
                                  float *lse, cudaStream_t stream);
 int b1_grid(int64_t n_rows, int num_sms);   // CTAs of the batch-1 kernel = its (max, sum exp) pairs
 
+// One-thread kernel whose bounded wait on a never-completed mbarrier gives up
+// and sets kStatusWaitTimeout in *status.
+cudaError_t launch_wait_timeout_selftest(uint32_t *status, cudaStream_t stream);
+
 // Tensor-core path (batches 2..32): activation-package prep + tcgen05 kernel.
 bool tc_supported(int batch, int k);
 size_t tc_workspace_bytes(int k);

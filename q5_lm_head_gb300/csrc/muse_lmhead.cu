@@ -314,6 +314,22 @@ int muse_lmhead_device_status(muse_lmhead *h, uint32_t *status_out) {
   return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
 }
 
+int muse_lmhead_clear_device_status(muse_lmhead *h, void *stream) {
+  if (!h) return MUSE_ERR_NULL;
+  DeviceGuard g(h->device);
+  if (!g.ok) return MUSE_ERR_DEVICE;
+  const cudaError_t e = cudaMemsetAsync(h->ws.status, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
+}
+
+int muse_lmhead_selftest_wait_timeout(muse_lmhead *h, void *stream) {
+  if (!h) return MUSE_ERR_NULL;
+  DeviceGuard g(h->device);
+  if (!g.ok) return MUSE_ERR_DEVICE;
+  const cudaError_t e = muse::launch_wait_timeout_selftest(h->ws.status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
+}
+
 void muse_lmhead_destroy(muse_lmhead *h) {
   if (!h) return;
   DeviceGuard g(h->device);

@@ -245,6 +245,8 @@ WORKLOADS: dict[str, Workload] = {
 }
 for _b in (1, 2, 4, 8, 16, 32):
     WORKLOADS[f"sweep_b{_b}"] = _lm(f"sweep_b{_b}", _b)
+# the DFlash verify batch: the target model scores the 16 drafted positions at once
+WORKLOADS["dflash_verify_b16"] = _lm("dflash_verify_b16", 16, BOOSTED_ROWS, (0.5, 4.0))
 # the Q4_K head alternative (756.5 MB), batch 1, same shapes and boosted rows
 WORKLOADS["lmhead_q4k_b1"] = Workload("lmhead_q4k_b1", VOCAB, HIDDEN, 1, "W:lmhead_q4k", boost_rows=BOOSTED_ROWS,
                                       hidden_tag="H:lmhead_q4k_b1", fmt="q4_k")
