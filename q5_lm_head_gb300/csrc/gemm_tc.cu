@@ -1,7 +1,7 @@
 // Batched output stage on the 5th-generation tensor cores (tcgen05), for
-// batches of 2..32 rows: final RMSNorm, Q5_K LM-head contraction, scale + soft
-// cap, argmax ("Chapter 20 — Final norm, LM head, and the soft cap", §20.1,
-// §20.3, §20.4).  Two launches per forward:
+// batches of 2..32 rows: final RMSNorm, Q5_K (or Q4_K) LM-head contraction,
+// scale + soft cap, argmax ("Chapter 20 — Final norm, LM head, and the soft
+// cap", §20.1, §20.3, §20.4, §20.8).  Two launches per forward:
 //
 // 1. prep_x_kernel: one CTA per (Q5_K block column kb, package row b).
 //    Normalises hidden row b and writes its part of the block's "activation
@@ -17,7 +17,7 @@
 //    programmatic dependent launch: everything but the package loads (set-up,
 //    the weight stream, the first unpack steps) overlaps the prep kernel.
 //    * weight producer warp: per block kb, one 2-D TMA box of 128 rows x 176
-//      bytes into a ring of weight stages.  Package producer warp: the kb
+//      bytes (144 for Q4_K) into a ring of weight stages.  Package producer warp: the kb
 //      activation package (1-D bulk copy) into a ring of package stages.
 //    * four unpack warpgroups in two pairs; pair p takes the blocks whose step
 //      index has parity p, so the two pairs work on consecutive blocks at once
@@ -52,7 +52,6 @@ namespace muse {
 namespace {
 
 constexpr int kTileRows = 128;                          // M of one MMA
-constexpr int kWStageBytes = kTileRows * kBlockBytes;   // 22,528: one block of a tile
 constexpr int kUnpackWarps = 16;                        // 2 pairs x 2 warpgroups
 constexpr int kThreads = 32 * (kUnpackWarps + 3);       // + weight producer, MMA issuer, package producer
 constexpr int kProducerWarp = kUnpackWarps;
@@ -65,9 +64,13 @@ constexpr int kSmemLimit = 227 * 1024 - 1024;           // opt-in limit minus st
 template <int NM>
 __host__ __device__ constexpr int min_rows() { return NM < 16 ? 16 : NM; }
 
-template <int NM>
+// NM batch slots; kQ4: Q4_K weight blocks (144 bytes) instead of Q5_K (176).
+// The activation package does not depend on the weight format.
+template <int NM, bool kQ4 = false>
 struct TcCfg {
   static_assert(NM == 8 || NM == 16 || NM == 32, "MMA N / 2");
+  static constexpr int kBB = kQ4 ? kBlockBytesQ4 : kBlockBytes;   // bytes per block
+  static constexpr int kWStageBytes = kTileRows * kBB;            // one block column of a tile
   static constexpr int kXRows = 2 * NM;                           // x_hi rows, then x_lo rows
   static constexpr int kXBytes = kXRows * kBlockWeights * 2;      // f16 [2NM][256] operand tile
   static constexpr int kMinBytes = min_rows<NM>() * 16 * 2;       // f16 [rows][16]
@@ -220,27 +223,35 @@ __device__ __forceinline__ void amin_cols(const RowHdr &h, uint32_t (&o)[8]) {
 
 // Columns 32c..32c+31 of A for one row: sub-blocks 2c (low nibbles, built as q)
 // and 2c+1 (high nibbles, built as 2q), as f16 pairs sc_s*q in natural K order;
-// stored to tensor memory at column `ta` in two 16-column halves.
+// stored to tensor memory at column `ta` in two 16-column halves.  Q5_K adds
+// each quant's fifth bit from the 32 high-bit bytes; Q4_K has none.
+template <bool kQ4>
 __device__ __forceinline__ void a_chunk_st(const uint8_t *blk, const RowHdr &h, int c, uint32_t ta) {
   const uint32_t scw = c < 2 ? h.sc03 : h.sc47;
   const uint32_t sh = 16u * (c & 1);
   const float sc_lo = static_cast<float>((scw >> sh) & 0xFFu);
   const float sc_hi = static_cast<float>((scw >> (sh + 8)) & 0xFFu);
-  const uint4 a0 = *reinterpret_cast<const uint4 *>(blk + kOffQs + 32 * c);
-  const uint4 a1 = *reinterpret_cast<const uint4 *>(blk + kOffQs + 32 * c + 16);
+  constexpr int kQs = kQ4 ? kOffQsQ4 : kOffQs;
+  const uint4 a0 = *reinterpret_cast<const uint4 *>(blk + kQs + 32 * c);
+  const uint4 a1 = *reinterpret_cast<const uint4 *>(blk + kQs + 32 * c + 16);
   const uint32_t A[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-  const uint4 h0 = *reinterpret_cast<const uint4 *>(blk + kOffQh);
-  const uint4 h1 = *reinterpret_cast<const uint4 *>(blk + kOffQh + 16);
-  uint32_t H[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-  const uint32_t rot = static_cast<uint32_t>(4 - 2 * c) & 31u;   // bit 2c -> 4, bit 2c+1 -> 5
+  uint32_t H[8] = {};
+  if constexpr (!kQ4) {
+    const uint4 h0 = *reinterpret_cast<const uint4 *>(blk + kOffQh);
+    const uint4 h1 = *reinterpret_cast<const uint4 *>(blk + kOffQh + 16);
+    H[0] = h0.x; H[1] = h0.y; H[2] = h0.z; H[3] = h0.w;
+    H[4] = h1.x; H[5] = h1.y; H[6] = h1.z; H[7] = h1.w;
+    const uint32_t rot = static_cast<uint32_t>(4 - 2 * c) & 31u;   // bit 2c -> 4, bit 2c+1 -> 5
 #pragma unroll
-  for (int i = 0; i < 8; ++i) H[i] = rotl32(H[i], rot);
+    for (int i = 0; i < 8; ++i) H[i] = rotl32(H[i], rot);
+  }
   uint32_t o[16];
   {
     const uint32_t mul = h2_bits(sc_lo), add = h2_bits(-1024.0f * sc_lo);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t q = (A[i] & 0x0F0F0F0Fu) | (H[i] & 0x10101010u);          // q, positions 4i..4i+3
+      uint32_t q = A[i] & 0x0F0F0F0Fu;                                        // q, positions 4i..4i+3
+      if constexpr (!kQ4) q |= H[i] & 0x10101010u;
       o[2 * i] = hfma2_u32(magic_pair<0>(q), mul, add);
       o[2 * i + 1] = hfma2_u32(magic_pair<2>(q), mul, add);
     }
@@ -250,7 +261,8 @@ __device__ __forceinline__ void a_chunk_st(const uint8_t *blk, const RowHdr &h, 
     const uint32_t mul = h2_bits(0.5f * sc_hi), add = h2_bits(-512.0f * sc_hi);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t q = ((A[i] >> 3) & 0x1E1E1E1Eu) | (H[i] & 0x20202020u);   // 2q
+      uint32_t q = (A[i] >> 3) & 0x1E1E1E1Eu;                                 // 2q
+      if constexpr (!kQ4) q |= H[i] & 0x20202020u;
       o[2 * i] = hfma2_u32(magic_pair<0>(q), mul, add);
       o[2 * i + 1] = hfma2_u32(magic_pair<2>(q), mul, add);
     }
@@ -266,16 +278,16 @@ __device__ __forceinline__ void ld_x4(uint32_t ta, uint32_t (&v)[4]) {
 }
 
 // ------------------------------------------------------------------ main kernel
-template <int NM>
+template <int NM, bool kQ4>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const uint8_t *__restrict__ pkgs, int nb,
                    int64_t n_rows, int batch, float scale, float cap, float *__restrict__ logits,
                    unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status) {
-  using C = TcCfg<NM>;
+  using C = TcCfg<NM, kQ4>;
   constexpr int HB = NM / 2;                                      // batch columns per warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t *wst = smem;                                            // [kWStages][128 rows][176 B]
-  uint8_t *xst = smem + C::kWStages * kWStageBytes;               // [C::kXStages][package]
+  uint8_t *wst = smem;                                            // [kWStages][128 rows][block bytes]
+  uint8_t *xst = smem + C::kWStages * C::kWStageBytes;            // [C::kXStages][package]
   float *xchg = reinterpret_cast<float *>(xst + C::kXStages * C::kPkgBytes);   // [2 halves][128][HB]
   uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) + C::kXchgBytes);
   uint64_t *wfull = bars, *wempty = bars + C::kWStages;
@@ -338,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t row0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
       for (int64_t g = 0; g < total && !*s_abort; ++g) {
         if (g >= C::kWStages && !ptx::mbar_wait(&wempty[ws], ph ^ 1u)) { fail(); break; }
-        ptx::mbar_arrive_expect_tx(&wfull[ws], kWStageBytes);
-        tma_load_2d(wst + ws * kWStageBytes, &wmap, kb * (kBlockBytes / 4), static_cast<int>(row0), &wfull[ws],
+        ptx::mbar_arrive_expect_tx(&wfull[ws], C::kWStageBytes);
+        tma_load_2d(wst + ws * C::kWStageBytes, &wmap, kb * (C::kBB / 4), static_cast<int>(row0), &wfull[ws],
                     pol_w);
         issued = g + 1;
         if (++ws == C::kWStages) { ws = 0; ph ^= 1u; }
@@ -490,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok_all = false;
         break;
       }
-      const uint8_t *blk = wst + ws * kWStageBytes + r * kBlockBytes;
+      const uint8_t *blk = wst + ws * C::kWStageBytes + r * C::kBB;
       RowHdr hd;
       load_row_hdr(blk, hd);
       const uint32_t ta = tbase + lane_base + C::col_a(p) + 64 * hf;
@@ -507,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      a_chunk_st(blk, hd, 2 * hf, ta);
-      a_chunk_st(blk, hd, 2 * hf + 1, ta + 32);
+      a_chunk_st<kQ4>(blk, hd, 2 * hf, ta);
+      a_chunk_st<kQ4>(blk, hd, 2 * hf + 1, ta + 32);
       if (hf == 0) {
         uint32_t am[8];
         amin_cols(hd, am);
@@ -565,16 +577,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
-template <int NM>
+template <int NM, bool kQ4>
 cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
-  using C = TcCfg<NM>;
+  using C = TcCfg<NM, kQ4>;
   static unsigned long long configured = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured & bit)) {
-    e = cudaFuncSetAttribute(gemm_tc_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    e = cudaFuncSetAttribute(gemm_tc_kernel<NM, kQ4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
@@ -595,7 +608,7 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NM>, map, static_cast<const uint8_t *>(a.ws.xpkg), nb,
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NM, kQ4>, map, static_cast<const uint8_t *>(a.ws.xpkg), nb,
                             a.n_rows, a.batch, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax,
                             a.ws.status);
 }
@@ -604,20 +617,23 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
 
 size_t tc_workspace_bytes(int k) { return static_cast<size_t>(k / kBlockWeights) * TcCfg<32>::kPkgBytes; }
 
-// Batches 2..32 with an even number of Q5_K blocks per row (both pairs of
-// unpack warpgroups then own blocks of every tile).
+// Batches 2..32 with an even number of blocks per row (both pairs of unpack
+// warpgroups then own blocks of every tile), either weight format.
 bool tc_supported(int batch, int k) {
   const int nb = k / kBlockWeights;
   return batch >= 2 && batch <= 32 && nb >= 2 && nb % 2 == 0;
 }
 
-cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_rows, int k) {
+cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_rows, int k, bool q4) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encoder();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k / kBlockWeights) * (kBlockBytes / 4),
+  // 32-bit elements: a block (176 or 144 bytes, both multiples of 16) is the
+  // box's inner extent, so every box starts on a 16-byte boundary
+  const int bb = q4 ? kBlockBytesQ4 : kBlockBytes;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k / kBlockWeights) * (bb / 4),
                               static_cast<cuuint64_t>(n_rows)};
-  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(k / kBlockWeights) * kBlockBytes};
-  const cuuint32_t box[2] = {kBlockBytes / 4, kTileRows};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(k / kBlockWeights) * bb};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(bb / 4), kTileRows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(weights), gdim, gstride, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -626,9 +642,14 @@ cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_r
 }
 
 cudaError_t launch_tc(const LaunchArgs &a, const CUtensorMap &map) {
-  if (a.batch <= 8) return launch_tc_nm<8>(a, map);
-  if (a.batch <= 16) return launch_tc_nm<16>(a, map);
-  return launch_tc_nm<32>(a, map);
+  if (a.q4) {
+    if (a.batch <= 8) return launch_tc_nm<8, true>(a, map);
+    if (a.batch <= 16) return launch_tc_nm<16, true>(a, map);
+    return launch_tc_nm<32, true>(a, map);
+  }
+  if (a.batch <= 8) return launch_tc_nm<8, false>(a, map);
+  if (a.batch <= 16) return launch_tc_nm<16, false>(a, map);
+  return launch_tc_nm<32, false>(a, map);
 }
 
 }  // namespace muse

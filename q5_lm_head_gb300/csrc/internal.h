@@ -77,7 +77,7 @@ cudaError_t launch_wait_timeout_selftest(uint32_t *status, cudaStream_t stream);
 // Tensor-core path (batches 2..32): activation-package prep + tcgen05 kernel.
 bool tc_supported(int batch, int k);
 size_t tc_workspace_bytes(int k);
-cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_rows, int k);
+cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_rows, int k, bool q4);
 cudaError_t launch_tc(const LaunchArgs &a, const CUtensorMap &map);
 
 }  // namespace muse

@@ -59,7 +59,7 @@ enum class Path { B1, TensorCore, Generic };
 
 Path choose_path(const muse_lmhead *h, int batch) {
   if (batch == 1 && muse::b1_supported(static_cast<int>(h->k))) return Path::B1;
-  if (h->format == MUSE_FORMAT_Q5_K && muse::tc_supported(batch, static_cast<int>(h->k))) return Path::TensorCore;
+  if (muse::tc_supported(batch, static_cast<int>(h->k))) return Path::TensorCore;
   return Path::Generic;
 }
 
@@ -100,7 +100,7 @@ int run_forward(muse_lmhead *h, const float *hidden, int batch, const float *gam
     case Path::B1: e = muse::launch_b1(a); break;
     case Path::TensorCore:
       if (h->wmap_ptr != weights) {
-        e = muse::tc_encode_weights(&h->wmap, weights, h->n_rows, static_cast<int>(h->k));
+        e = muse::tc_encode_weights(&h->wmap, weights, h->n_rows, static_cast<int>(h->k), a.q4);
         if (e != cudaSuccess) break;
         h->wmap_ptr = weights;
       }

@@ -15,6 +15,8 @@ attention projections of "Chapter 9 — The Muse Glimmer architecture" §9.3):
 * ``lmhead_b8``   B=8, same weights; hidden rows scaled by U(0.5, 4)
 * ``attn_q`` ``attn_k`` ``attn_v`` ``attn_o``  projection shapes, B=1, no norm/scale/cap
 * ``sweep_b{1,2,4,8,16,32}``  N=202,048 x 6,656, no boosted rows
+* ``dflash_verify_b16``  B=16 (the drafted positions), rows scaled by U(0.5, 4)
+* ``lmhead_q4k_b1`` ``lmhead_q4k_b8``  the Q4_K head (756.5 MB), B=1 and B=8
 """
 from __future__ import annotations
 
@@ -250,6 +252,8 @@ WORKLOADS["dflash_verify_b16"] = _lm("dflash_verify_b16", 16, BOOSTED_ROWS, (0.5
 # the Q4_K head alternative (756.5 MB), batch 1, same shapes and boosted rows
 WORKLOADS["lmhead_q4k_b1"] = Workload("lmhead_q4k_b1", VOCAB, HIDDEN, 1, "W:lmhead_q4k", boost_rows=BOOSTED_ROWS,
                                       hidden_tag="H:lmhead_q4k_b1", fmt="q4_k")
+WORKLOADS["lmhead_q4k_b8"] = Workload("lmhead_q4k_b8", VOCAB, HIDDEN, 8, "W:lmhead_q4k", boost_rows=BOOSTED_ROWS,
+                                      row_scale=(0.5, 4.0), hidden_tag="H:lmhead_q4k_b8", fmt="q4_k")
 
 
 @dataclass(frozen=True)

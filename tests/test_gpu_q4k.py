@@ -4,7 +4,8 @@ LM head, and the soft cap" §20.8) against the f64 oracle's own Q4_K parser.
 
 Same bar as Q5_K: |gpu - oracle| <= 2e-3 on every logit, argmax equal where
 the oracle's top-2 gap exceeds 4e-3.  Covers the fused batch-1 kernel (K =
-6,656 and 4,096), the generic kernel (batches > 1, other K) and the logprobs
+6,656 and 4,096), the tensor-core kernel (batches 2..32, an even number of
+blocks per row), the generic kernel (the other shapes) and the logprobs
 forward.
 """
 import numpy as np
@@ -68,33 +69,48 @@ def test_q4k_full_head_batch1(torch_cuda):
     _check(got, am, oracle.lmhead(hidden, gamma, wq, wl.scale, wl.cap, synth.RMS_EPS, fmt="q4_k"))
 
 
-@pytest.mark.parametrize("n,k,b,norm,cap", [
-    (777, 4096, 1, True, 20.0),     # fused kernel, K = 4,096
-    (25, 6656, 1, False, 0.0),      # fewer rows than one stage per CTA
-    (3001, 6656, 3, True, 20.0),    # generic kernel (the tensor-core path reads Q5_K only)
-    (500, 512, 1, True, 20.0),      # generic kernel, K with no fused kernel
-    (64, 768, 8, False, 0.0),
+def test_q4k_full_head_batch8(torch_cuda):
+    wl = synth.WORKLOADS["lmhead_q4k_b8"]        # same weights as the batch-1 head, rows scaled by U(0.5, 4)
+    hidden, gamma, wq = synth.inputs_for(wl)
+    got, am = _run(torch_cuda, hidden, gamma, wq, wl.n_rows, wl.k, wl.scale, wl.cap, "gemm_tc")
+    ref = oracle.lmhead(hidden, gamma, wq, wl.scale, wl.cap, synth.RMS_EPS, fmt="q4_k")
+    _check(got, am, ref)
+    for r in synth.BOOSTED_ROWS:                 # past the cap's knee
+        assert np.abs(ref[:, r]).max() > 19.0 and np.abs(got[:, r]).max() <= 20.0
+
+
+@pytest.mark.parametrize("n,k,b,norm,cap,path", [
+    (777, 4096, 1, True, 20.0, "gemv_b1"),      # fused kernel, K = 4,096
+    (25, 6656, 1, False, 0.0, "gemv_b1"),       # fewer rows than one stage per CTA
+    (3001, 6656, 3, True, 20.0, "gemm_tc"),     # ragged last 128-row tile
+    (129, 6656, 2, False, 0.0, "gemm_tc"),      # one row past a tile, cap off
+    (5000, 4096, 16, True, 20.0, "gemm_tc"),
+    (1000, 512, 32, True, 20.0, "gemm_tc"),     # two blocks per row, 32 batch rows
+    (500, 512, 1, True, 20.0, "gemv_generic"),  # K with no fused kernel
+    (64, 768, 8, False, 0.0, "gemv_generic"),   # odd number of blocks per row
 ])
-def test_q4k_shapes(torch_cuda, n, k, b, norm, cap):
+def test_q4k_shapes(torch_cuda, n, k, b, norm, cap, path):
     rng = np.random.default_rng(n * 7 + k + b)
     hidden = rng.standard_normal((b, k)).astype(np.float32)
     gamma = (1.0 + 0.1 * rng.standard_normal(k)).astype(np.float32) if norm else None
     wq = synth.q5k_matrix(n, k, synth.stream_key(9, f"W:q4:{n}:{k}"), boost_rows=(n // 2,), boost=50.0,
                           fmt="q4_k")
     scale = synth.LOGIT_SCALE if cap > 0 else 1.0
-    got, am = _run(torch_cuda, hidden, gamma, wq, n, k, scale, cap)
+    got, am = _run(torch_cuda, hidden, gamma, wq, n, k, scale, cap, path)
     _check(got, am, oracle.lmhead(hidden, gamma, wq, scale, cap, synth.RMS_EPS, fmt="q4_k"))
 
 
-def test_q4k_logprobs_batch1(torch_cuda):
+@pytest.mark.parametrize("b", [1, 4])
+def test_q4k_logprobs(torch_cuda, b):
     import q5_lm_head_gb300 as mlh
     torch = torch_cuda
     n, k = 30000, 6656
-    rng = np.random.default_rng(5)
-    hidden = rng.standard_normal((1, k)).astype(np.float32)
+    rng = np.random.default_rng(5 + b)
+    hidden = rng.standard_normal((b, k)).astype(np.float32)
     gamma = (1.0 + 0.1 * rng.standard_normal(k)).astype(np.float32)
     wq = synth.q5k_matrix(n, k, synth.stream_key(10, "W:q4lp"), fmt="q4_k")
-    with mlh.LMHead(n, k, max_batch=1, device=0, fmt="q4_k") as head:
+    with mlh.LMHead(n, k, max_batch=b, device=0, fmt="q4_k") as head:
+        assert head.path_name(b) == ("gemv_b1" if b == 1 else "gemm_tc")
         lp, lse, am = head.forward_logprobs(_dev(torch, hidden), _dev(torch, wq), _dev(torch, gamma))
         torch.cuda.synchronize()
         lp, lse = lp.cpu().numpy(), lse.cpu().numpy()
