@@ -163,8 +163,10 @@ const char *muse_lmhead_path_name(const muse_lmhead *h, int batch);
 int muse_lmhead_device_status(muse_lmhead *h, uint32_t *status_out);
 
 /*
- * Clear the handle's status word (asynchronous 4-byte memset on `stream`), for
- * example after a recorded timeout, once the caller has dealt with it.
+ * Clear the handle's status word (asynchronous memsets on `stream`), for
+ * example after a recorded timeout, once the caller has dealt with it.  Also
+ * re-arms the tensor-core path's per-boundary arrival counters, which a
+ * forward that gave up may have left counted in.
  */
 int muse_lmhead_clear_device_status(muse_lmhead *h, void *stream);
 

@@ -88,6 +88,17 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) 
   return ((unsigned long long)float_order_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
 }
 
+// The warp's largest argmax_key over its lanes' (v, idx), or 0 where no lane
+// is valid: the highest value bits first, then the highest index bits among
+// the lanes holding them (two warp reductions instead of a 64-bit butterfly).
+__device__ __forceinline__ unsigned long long warp_argmax_key(float v, uint32_t idx, bool valid) {
+  const uint32_t hi = valid ? float_order_key(v) : 0u;
+  const uint32_t lo = valid ? 0xFFFFFFFFu - idx : 0u;
+  const uint32_t m_hi = __reduce_max_sync(0xffffffffu, hi);
+  const uint32_t m_lo = __reduce_max_sync(0xffffffffu, hi == m_hi ? lo : 0u);
+  return ((unsigned long long)m_hi << 32) | m_lo;
+}
+
 __device__ __forceinline__ uint32_t argmax_key_index(unsigned long long key) {
   return 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
 }

@@ -16,6 +16,13 @@
 // 2. gemm_tc_kernel: a persistent CTA per SM works on 128-row tiles.  It is a
 //    programmatic dependent launch: everything but the package loads (set-up,
 //    the weight stream, the first unpack steps) overlaps the prep kernel.
+//    With up to 16 batch slots the (tile, block) steps are dealt out as equal
+//    contiguous ranges (in pairs of steps), so every CTA streams the same
+//    number of blocks; a tile cut by a range boundary is shared by two
+//    neighbouring CTAs, which both leave their partial sums in global memory
+//    and count in; the second to arrive adds the two (in a fixed order) and
+//    finishes the rows.  With 32 slots the hand-off of the 32 partial columns
+//    costs more than the balance gains (measured), and tiles go round-robin.
 //    * weight producer warp: per block kb, one 2-D TMA box of 128 rows x 176
 //      bytes (144 for Q4_K) into a ring of weight stages.  Package producer warp: the kb
 //      activation package (1-D bulk copy) into a ring of package stages.
@@ -282,7 +289,8 @@ template <int NM, bool kQ4>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const uint8_t *__restrict__ pkgs, int nb,
                    int64_t n_rows, int batch, float scale, float cap, float *__restrict__ logits,
-                   unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status) {
+                   unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status,
+                   float *split_part, unsigned int *split_cnt) {
   using C = TcCfg<NM, kQ4>;
   constexpr int HB = NM / 2;                                      // batch columns per warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -302,8 +310,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t n_tiles = (n_rows + kTileRows - 1) / kTileRows;
-  const int64_t my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int64_t total = my_tiles * nb;                            // (tile, block) steps of this CTA
+  // Balanced: this CTA's steps [s_begin, s_end) of the tile-major (tile,
+  // block) sequence, equal shares in pairs of steps (nb is even, so both pairs
+  // keep their parity across tiles).  With at most n_tiles CTAs a share is at
+  // least nb steps, so a tile is cut at most once and shared by at most two
+  // CTAs.  Round-robin: tiles blockIdx.x + j * gridDim.x, none shared.
+  constexpr bool kBalanced = NM <= 16;
+  int64_t total, tile_first, tile_last = -1, tile_step = 1;
+  int kb_first = 0, kb_end = 0;                                   // kb_end 0: the range ends on a tile boundary
+  if constexpr (kBalanced) {
+    const int64_t pairs = n_tiles * (nb / 2);
+    const int64_t s_begin = 2 * (pairs * blockIdx.x / gridDim.x);
+    const int64_t s_end = 2 * (pairs * (blockIdx.x + 1) / gridDim.x);
+    total = s_end - s_begin;
+    tile_first = s_begin / nb;
+    kb_first = static_cast<int>(s_begin - tile_first * nb);         // even
+    tile_last = (s_end - 1) / nb;
+    kb_end = static_cast<int>(s_end - (s_end / nb) * nb);
+  } else {
+    total = (blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0) * nb;
+    tile_first = blockIdx.x;
+    tile_step = gridDim.x;
+  }
 
   if (tid == 0) {
     for (int s = 0; s < C::kWStages; ++s) {
@@ -345,9 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = ptx::policy_evict_first();
       // step g = (tile, block kb) in tile-major order; counters instead of divisions
       int64_t issued = 0;
-      int kb = 0, ws = 0;
+      int kb = kb_first, ws = 0;
       uint32_t ph = 0;                          // parity of the current pass over the ring
-      int64_t row0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
+      int64_t row0 = tile_first * kTileRows;
       for (int64_t g = 0; g < total && !*s_abort; ++g) {
         if (g >= C::kWStages && !ptx::mbar_wait(&wempty[ws], ph ^ 1u)) { fail(); break; }
         ptx::mbar_arrive_expect_tx(&wfull[ws], C::kWStageBytes);
@@ -355,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pol_w);
         issued = g + 1;
         if (++ws == C::kWStages) { ws = 0; ph ^= 1u; }
-        if (++kb == nb) { kb = 0; row0 += static_cast<int64_t>(gridDim.x) * kTileRows; }
+        if (++kb == nb) { kb = 0; row0 += tile_step * kTileRows; }
       }
       // never leave copies in flight
       for (int64_t g = issued > C::kWStages ? issued - C::kWStages : 0; g < issued; ++g)
@@ -367,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("griddepcontrol.wait;" ::: "memory");   // the prep grid has completed
 
       int64_t issued = 0;
-      int kb = 0, xs = 0;
+      int kb = kb_first, xs = 0;
       uint32_t ph = 0;
       for (int64_t g = 0; g < total && !*s_abort; ++g) {
         if (g >= C::kXStages && !ptx::mbar_wait(&xempty[xs], ph ^ 1u)) { fail(); break; }
@@ -452,9 +480,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     // End of a tile: pair 1 hands its sums to pair 0 through shared memory
-    // (bounded mbarrier handshake), pair 0 finishes the rows.
+    // (bounded mbarrier handshake), pair 0 finishes the rows.  A tile shared
+    // with a neighbouring CTA (this CTA's first tile: side 1 of boundary
+    // blockIdx.x - 1; its last: side 0 of boundary blockIdx.x) goes through
+    // the boundary's slot, warp by warp (32 rows): both CTAs' warps store
+    // their sums, then count in with one atomic per warp; the second adds
+    // side 0 + side 1 (the same order in either CTA) and finishes the rows.
     uint32_t n_fin = 0;
-    auto finish_tile = [&](int64_t row) -> bool {
+    auto finish_tile = [&](int64_t t) -> bool {
+      const int64_t row = t * kTileRows + r;
+      int side = -1;
+      uint32_t slot = 0;
+      if (t == tile_first && kb_first != 0) {
+        side = 1;
+        slot = blockIdx.x - 1;
+      } else if (t == tile_last && kb_end != 0) {
+        side = 0;
+        slot = blockIdx.x;
+      }
       float *xw = xchg + (hf * kTileRows + r) * HB;
       bool ok = true;
       if (p == 1) {
@@ -466,21 +509,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         ok = __all_sync(0xffffffffu, ptx::mbar_wait(xch_full, n_fin & 1u));
+        float v[HB];
+        bool store = ok;
         if (ok) {
+#pragma unroll
+          for (int b = 0; b < HB; ++b) v[b] = acc[b] + xw[b];
+          ptx::mbar_arrive(xch_empty);
+        }
+        if (ok && side >= 0) {
+          float *base = split_part + (static_cast<size_t>(slot) * 2 * kTileRows + r) * NM + b0;
+          float *mine = base + side * kTileRows * NM;
+#pragma unroll
+          for (int b = 0; b < HB; ++b) mine[b] = v[b];
+          __threadfence();                       // this lane's sums before the warp's count
+          __syncwarp();
+          uint32_t who = 0u;
+          unsigned int *cnt = split_cnt + slot * (kUnpackWarps / 2) + (warp & 7);
+          if (lane == 0) {
+            who = atomicAdd(cnt, 1u);
+            if (who == 1u) *cnt = 0u;            // both warps counted in: re-armed for the next launch
+          }
+          store = __shfl_sync(0xffffffffu, who, 0) == 1u;
+          if (store) {
+            __threadfence();                     // the other CTA's sums after its count
+            const float *other = base + (1 - side) * kTileRows * NM;
+#pragma unroll
+            for (int b = 0; b < HB; ++b) {
+              const float o = __ldcg(other + b);
+              v[b] = side == 0 ? v[b] + o : o + v[b];
+            }
+          }
+        }
+        if (store) {
 #pragma unroll
           for (int b = 0; b < HB; ++b) {
             if (b0 + b < batch) {
-              const float v = scale_softcap(acc[b] + xw[b], scale, cap);
-              unsigned long long key = 0ull;
-              if (row < n_rows) {
-                logits[static_cast<size_t>(b0 + b) * n_rows + row] = v;
-                key = argmax_key(v, static_cast<uint32_t>(row));
-              }
-              for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xffffffffu, key, o));
+              const float v_out = scale_softcap(v[b], scale, cap);
+              const bool valid = row < n_rows;
+              if (valid) logits[static_cast<size_t>(b0 + b) * n_rows + row] = v_out;
+              const unsigned long long key = warp_argmax_key(v_out, static_cast<uint32_t>(row), valid);
               if (lane == 0 && key != 0ull) atomicMax(&s_keys[b0 + b], key);
             }
           }
-          ptx::mbar_arrive(xch_empty);
         }
       }
       ++n_fin;
@@ -491,9 +561,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok_all = true;
     // The pair's steps g = p, p+2, ...: weight stage, ring parity, block and
     // tile follow by counting (nb and the ring size are even).
-    int ws = p, kb = p;
+    int ws = p, kb = kb_first + p;
     uint32_t wph = 0;
-    int64_t tile = blockIdx.x, tile_prev = -1;
+    int64_t tile = tile_first, tile_prev = -1;
     uint32_t i = 0;                             // the pair's step count
     for (int64_t g = p; g < total; g += 2, ++i) {
       if (__any_sync(0xffffffffu, *s_abort != 0u)) { ok_all = false; break; }
@@ -513,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         drain();
-        if (tile != tile_prev && !finish_tile(tile_prev * kTileRows + r)) {   // that block closed a tile
+        if (tile != tile_prev && !finish_tile(tile_prev)) {   // that block closed a tile
           if (lane == 0) fail();
           ok_all = false;
           break;
@@ -536,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dmin_prev = hd.dmin;
       tile_prev = tile;
       if ((ws += 2) >= C::kWStages) { ws -= C::kWStages; wph ^= 1u; }
-      if ((kb += 2) >= nb) { kb -= nb; tile += gridDim.x; }
+      if ((kb += 2) >= nb) { kb -= nb; tile += tile_step; }
     }
     // The pair's last block and the last tile.  Both pairs get here having
     // taken part in the same tile hand-overs: nb is even, so each pair owns
@@ -544,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok_all && i > 0) {
       if (__all_sync(0xffffffffu, ptx::mbar_wait(&adone[p], (i - 1) & 1u))) {
         drain();
-        if (!finish_tile(tile_prev * kTileRows + r) && lane == 0) fail();
+        if (!finish_tile(tile_prev) && lane == 0) fail();
       } else if (lane == 0) {
         fail();
       }
@@ -610,12 +680,20 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NM, kQ4>, map, static_cast<const uint8_t *>(a.ws.xpkg), nb,
                             a.n_rows, a.batch, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax,
-                            a.ws.status);
+                            a.ws.status, a.ws.split_part, a.ws.split_cnt);
 }
 
 }  // namespace
 
 size_t tc_workspace_bytes(int k) { return static_cast<size_t>(k / kBlockWeights) * TcCfg<32>::kPkgBytes; }
+
+int tc_batch_slots(int batch) { return batch <= 8 ? 8 : batch <= 16 ? 16 : 32; }
+
+size_t tc_split_floats(int num_sms, int max_batch) {
+  return static_cast<size_t>(num_sms) * 2 * kTileRows * tc_batch_slots(max_batch);
+}
+
+size_t tc_split_counters(int num_sms) { return static_cast<size_t>(num_sms) * (kUnpackWarps / 2); }
 
 // Batches 2..32 with an even number of blocks per row (both pairs of unpack
 // warpgroups then own blocks of every tile), either weight format.
@@ -642,13 +720,14 @@ cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_r
 }
 
 cudaError_t launch_tc(const LaunchArgs &a, const CUtensorMap &map) {
+  const int nm = tc_batch_slots(a.batch);
   if (a.q4) {
-    if (a.batch <= 8) return launch_tc_nm<8, true>(a, map);
-    if (a.batch <= 16) return launch_tc_nm<16, true>(a, map);
+    if (nm == 8) return launch_tc_nm<8, true>(a, map);
+    if (nm == 16) return launch_tc_nm<16, true>(a, map);
     return launch_tc_nm<32, true>(a, map);
   }
-  if (a.batch <= 8) return launch_tc_nm<8, false>(a, map);
-  if (a.batch <= 16) return launch_tc_nm<16, false>(a, map);
+  if (nm == 8) return launch_tc_nm<8, false>(a, map);
+  if (nm == 16) return launch_tc_nm<16, false>(a, map);
   return launch_tc_nm<32, false>(a, map);
 }
 

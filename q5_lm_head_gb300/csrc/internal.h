@@ -19,6 +19,8 @@ struct Workspace {
   float *x;                  // [max_batch][k] normalised input (generic path)
   uint8_t *xpkg;             // per-block activation packages (tensor-core path)
   float2 *lse_parts;         // [MUSE_MAX_BATCH][kMaxLseParts] (max, sum exp) partials of the logprobs
+  float *split_part;         // tensor-core path: [num_sms][2][128][slots] partial sums of shared tiles
+  unsigned int *split_cnt;   // [num_sms][8] arrivals per shared tile and warp, zero between forwards
 };
 
 constexpr int kMaxLseParts = 256;
@@ -77,6 +79,9 @@ cudaError_t launch_wait_timeout_selftest(uint32_t *status, cudaStream_t stream);
 // Tensor-core path (batches 2..32): activation-package prep + tcgen05 kernel.
 bool tc_supported(int batch, int k);
 size_t tc_workspace_bytes(int k);
+int tc_batch_slots(int batch);                       // the kernel's batch slots (8, 16 or 32)
+size_t tc_split_floats(int num_sms, int max_batch);  // split_part size
+size_t tc_split_counters(int num_sms);                // split_cnt size
 cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_rows, int k, bool q4);
 cudaError_t launch_tc(const LaunchArgs &a, const CUtensorMap &map);
 

@@ -23,6 +23,7 @@ struct muse_lmhead {
   int num_sms;
   muse::Workspace ws;
   void *ws_base;           // single device allocation backing ws
+  size_t ws_split_cnt_bytes;  // size of ws.split_cnt (0 without the tensor-core path)
   CUtensorMap wmap;        // weight tensor map of the tensor-core path, for wmap_ptr
   const void *wmap_ptr;
   float *stage_hidden;     // forward_host staging (lazy)
@@ -147,13 +148,17 @@ int muse_lmhead_init_format(muse_lmhead **out, int device, int64_t n_rows, int64
   h->max_batch = max_batch;
   h->num_sms = prop.multiProcessorCount;
 
-  // One zeroed allocation: keys | ticket | status | logprob pairs | x | activation packages
+  // One zeroed allocation: keys | ticket | status | logprob pairs | x | activation packages |
+  // shared-tile counters | shared-tile partial sums (the last three for the tensor-core path)
   const size_t keys_b = sizeof(unsigned long long) * MUSE_MAX_BATCH;
   const size_t misc_b = 256;
   const size_t lse_b = sizeof(float2) * static_cast<size_t>(max_batch) * muse::kMaxLseParts;
   const size_t x_b = sizeof(float) * static_cast<size_t>(max_batch) * static_cast<size_t>(k);
-  const size_t pkg_b = max_batch >= 2 ? muse::tc_workspace_bytes(static_cast<int>(k)) : 0;
-  const size_t total = keys_b + misc_b + lse_b + x_b + pkg_b;
+  const bool tc = max_batch >= 2;
+  const size_t pkg_b = tc ? muse::tc_workspace_bytes(static_cast<int>(k)) : 0;
+  const size_t cnt_b = tc ? (sizeof(unsigned int) * muse::tc_split_counters(h->num_sms) + 255) / 256 * 256 : 0;
+  const size_t part_b = tc ? sizeof(float) * muse::tc_split_floats(h->num_sms, max_batch) : 0;
+  const size_t total = keys_b + misc_b + lse_b + x_b + pkg_b + cnt_b + part_b;
   void *base = nullptr;
   e = cudaMalloc(&base, total);
   if (e != cudaSuccess) {
@@ -174,6 +179,9 @@ int muse_lmhead_init_format(muse_lmhead **out, int device, int64_t n_rows, int64
   h->ws.lse_parts = reinterpret_cast<float2 *>(p + keys_b + misc_b);
   h->ws.x = reinterpret_cast<float *>(p + keys_b + misc_b + lse_b);
   h->ws.xpkg = pkg_b ? p + keys_b + misc_b + lse_b + x_b : nullptr;
+  h->ws.split_cnt = cnt_b ? reinterpret_cast<unsigned int *>(p + keys_b + misc_b + lse_b + x_b + pkg_b) : nullptr;
+  h->ws.split_part = part_b ? reinterpret_cast<float *>(p + keys_b + misc_b + lse_b + x_b + pkg_b + cnt_b) : nullptr;
+  h->ws_split_cnt_bytes = cnt_b;
   *out = h;
   return MUSE_OK;
 }
@@ -318,7 +326,10 @@ int muse_lmhead_clear_device_status(muse_lmhead *h, void *stream) {
   if (!h) return MUSE_ERR_NULL;
   DeviceGuard g(h->device);
   if (!g.ok) return MUSE_ERR_DEVICE;
-  const cudaError_t e = cudaMemsetAsync(h->ws.status, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaMemsetAsync(h->ws.status, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream));
+  // a forward that gave up may have left a shared-tile counter counted in
+  if (e == cudaSuccess && h->ws.split_cnt)
+    e = cudaMemsetAsync(h->ws.split_cnt, 0, h->ws_split_cnt_bytes, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
 }
 

@@ -133,6 +133,8 @@ CASES = [
     (4096, 6656, 5, True, 20.0, True),
     (777, 1024, 32, True, 20.0, True),
     (64, 4096, 16, True, 30.0, True),
+    (19600, 1024, 4, True, 20.0, True),     # more 128-row tiles than SMs: tiles shared by two CTAs
+    (57857, 1024, 3, False, 0.0, True),     # shared tiles and a one-row last tile
 ]
 
 
@@ -187,6 +189,31 @@ def test_repeat_calls_are_deterministic_and_rearm_argmax(torch_cuda):
     assert torch.equal(l1, l3) and torch.equal(a1, a3)
     ref2 = oracle.lmhead(hidden2, gamma, wq, wl.scale, wl.cap)
     assert_parity(l2.cpu().numpy(), a2.cpu().numpy(), ref2, "second input")
+
+
+def test_tensor_core_shared_tiles_repeat_bit_for_bit(torch_cuda):
+    """More tiles than SMs: CTAs share the tiles at their range boundaries and the
+    second to arrive finishes them.  Whichever CTA that is, the two partial sums
+    are added in a fixed order, and the arrival counters re-arm for the next call,
+    so repeated forwards (alternating inputs) give the same bits."""
+    import q5_lm_head_gb300 as mlh
+    torch = torch_cuda
+    n, k, b = 40000, 6656, 5
+    wq = synth.q5k_matrix(n, k, synth.stream_key(2, "W:shared"), boost_rows=(777,), boost=40.0)
+    hidden = synth.normal_f64(b * k, synth.stream_key(2, "H:shared")).astype(np.float32).reshape(b, k)
+    gamma = synth.normal_f64(k, synth.stream_key(2, "G:shared"), 1.0, 0.1).astype(np.float32)
+    with mlh.LMHead(n, k, max_batch=b, device=0) as head:
+        assert head.path_name(b) == "gemm_tc"
+        h1, h2 = _dev(torch, hidden), _dev(torch, hidden[::-1].copy())
+        w_d, g_d = _dev(torch, wq), _dev(torch, gamma)
+        outs = [[t.clone() for t in head.forward(h, w_d, g_d)] for h in (h1, h2, h1, h2, h1)]
+        torch.cuda.synchronize()
+        assert head.device_status() == 0
+    for i in (2, 4):
+        assert torch.equal(outs[0][0], outs[i][0]) and torch.equal(outs[0][1], outs[i][1])
+    assert torch.equal(outs[1][0], outs[3][0])
+    ref = oracle.lmhead(hidden, gamma, wq, synth.LOGIT_SCALE, synth.SOFTCAP, synth.RMS_EPS)
+    assert_parity(outs[0][0].cpu().numpy(), outs[0][1].cpu().numpy(), ref, "shared tiles")
 
 
 def test_forward_host_matches_device_forward(torch_cuda):
