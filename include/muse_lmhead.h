@@ -128,12 +128,16 @@ int muse_lmhead_forward_logprobs(muse_lmhead *h, const float *hidden, int batch,
 
 /*
  * The same forward for callers whose activations live in host memory: copies
- * hidden_host to the device, runs the forward, copies the logits (and argmax)
+ * hidden_host to the device, runs the forward, brings the logits (and argmax)
  * back, and waits for `stream` before returning.  gamma and weights are device
  * pointers (they stay resident).  logits_host may be NULL to fetch only the
- * argmax; argmax_host may be NULL to skip it.  Host buffers should be pinned
- * (page-locked) for full copy bandwidth; pageable memory also works.  The first
- * call allocates the handle's device staging buffers (max_batch rows).
+ * argmax; argmax_host may be NULL to skip it.  An output buffer that is
+ * page-locked for this device (cudaHostAlloc, cudaHostRegister) is written by
+ * the kernels directly through the device's mapping of host memory, with no
+ * copy after the kernels; a pageable one is filled from a device staging
+ * buffer by a copy.  The input should be page-locked for full copy bandwidth;
+ * pageable memory also works.  The first call allocates the handle's device
+ * staging buffers (max_batch rows).
  */
 int muse_lmhead_forward_host(muse_lmhead *h, const float *hidden_host, int batch,
                              const float *gamma, float eps, const void *weights,

@@ -247,6 +247,23 @@ int muse_lmhead_forward(muse_lmhead *h, const float *hidden, int batch, const fl
                      static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+// The device's address of a page-locked host buffer (cudaHostAlloc or
+// cudaHostRegister memory mapped for this handle's device), or nullptr for
+// pageable memory and memory pinned for another device's context.
+void *mapped_alias(const void *p, int device) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();                   // clear the sticky-free error of an unknown pointer
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer || at.device != device) return nullptr;
+  return at.devicePointer;
+}
+
+}  // namespace
+
 int muse_lmhead_forward_host(muse_lmhead *h, const float *hidden_host, int batch, const float *gamma,
                              float eps, const void *weights, float scale, float cap, float *logits_host,
                              int32_t *argmax_host, void *stream) {
@@ -278,8 +295,20 @@ int muse_lmhead_forward_host(muse_lmhead *h, const float *hidden_host, int batch
   const size_t in_b = sizeof(float) * static_cast<size_t>(batch) * h->k;
   if ((e = cudaMemcpyAsync(h->stage_hidden, hidden_host, in_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
     return cuda_fail(e);
-  st = run_forward(h, h->stage_hidden, batch, gamma, eps, weights, scale, cap, h->stage_logits,
-                   argmax_host ? h->stage_argmax : nullptr, s);
+  // Page-locked output buffers are written by the kernels themselves, through
+  // the device's mapping of host memory (the link carries the same bytes, with
+  // no copy after the kernel); pageable ones go through the staging buffers.
+  float *logits_out = h->stage_logits;              // the kernels' logits when none reach the host
+  int32_t *argmax_out = argmax_host ? h->stage_argmax : nullptr;
+  if (void *a = logits_host ? mapped_alias(logits_host, h->device) : nullptr) {
+    logits_out = static_cast<float *>(a);
+    logits_host = nullptr;                           // nothing left to copy
+  }
+  if (void *a = argmax_host ? mapped_alias(argmax_host, h->device) : nullptr) {
+    argmax_out = static_cast<int32_t *>(a);
+    argmax_host = nullptr;
+  }
+  st = run_forward(h, h->stage_hidden, batch, gamma, eps, weights, scale, cap, logits_out, argmax_out, s);
   if (st != MUSE_OK) return st;
   if (logits_host) {
     const size_t out_b = sizeof(float) * static_cast<size_t>(batch) * h->n_rows;

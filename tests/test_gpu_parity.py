@@ -224,9 +224,21 @@ def test_forward_host_matches_device_forward(torch_cuda):
     with mlh.LMHead(wl.n_rows, wl.k, max_batch=4, device=0) as head:
         w_d, g_d = _dev(torch, wq), _dev(torch, gamma)
         ld, ad = head.forward(_dev(torch, hidden), w_d, g_d)
+        # page-locked outputs (written by the kernels through the host mapping)
         lh, ah = head.forward_host(torch.from_numpy(hidden).pin_memory(), w_d, g_d)
+        # pageable outputs and input (staged in device memory, copied back)
+        lp = torch.full((1, wl.n_rows), float("nan"))
+        ap = torch.full((1,), -1, dtype=torch.int32)
+        head.forward_host(torch.from_numpy(hidden.copy()), w_d, g_d, logits_host=lp, argmax_host=ap)
+        # argmax only, into page-locked memory
+        ao = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+        st = mlh.muse_lmhead_forward_host(head.handle, torch.from_numpy(hidden).pin_memory().data_ptr(), 1,
+                                          g_d.data_ptr(), synth.RMS_EPS, w_d.data_ptr(), synth.LOGIT_SCALE,
+                                          synth.SOFTCAP, None, ao.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert st == 0
         torch.cuda.synchronize()
     assert torch.equal(ld.cpu(), lh) and torch.equal(ad.cpu(), ah)
+    assert torch.equal(ld.cpu(), lp) and torch.equal(ad.cpu(), ap) and torch.equal(ad.cpu(), ao)
 
 
 def test_two_handles_on_two_streams(torch_cuda):
