@@ -102,22 +102,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ncu summaries that carry a per-launch DRAM traffic figure: (file, workload, kernel sources)
-_PROFILED = {"gemv_b1": ("gemv_b1_lmhead.md", "lmhead_b1", ("gemv_b1.cu", "common.cuh", "ptx.cuh")),
-             "gemm_tc": ("gemm_tc_lmhead_b8.md", "lmhead_b8", ("gemm_tc.cu", "common.cuh", "ptx.cuh", "tc.cuh")),
-             "gemv_b1_group": ("gemv_b1_group_attn_qkvg.md", "attn_qkvg", ("gemv_b1.cu", "common.cuh", "ptx.cuh"))}
+# ncu summaries that carry a per-launch DRAM traffic figure:
+# (kernel path, workload) -> (file, kernel sources)
+_B1_SRC = ("gemv_b1.cu", "common.cuh", "ptx.cuh")
+_PROFILED = {("gemv_b1", "lmhead_b1"): ("gemv_b1_lmhead.md", _B1_SRC),
+             ("gemv_b1", "lmhead_q4k_b1"): ("gemv_b1_lmhead_q4k.md", _B1_SRC),
+             ("gemm_tc", "lmhead_b8"): ("gemm_tc_lmhead_b8.md", ("gemm_tc.cu", "common.cuh", "ptx.cuh", "tc.cuh")),
+             ("gemv_b1_group", "attn_qkvg"): ("gemv_b1_group_attn_qkvg.md", _B1_SRC)}
 
 
 def _profiled_traffic(kernel_path: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, or None when there
     is none for this kernel/workload or the kernel source changed since."""
     import hashlib
-    ent = _PROFILED.get(kernel_path)
-    if not ent or ent[1] != workload:
+    ent = _PROFILED.get((kernel_path, workload))
+    if not ent:
         return None
     csrc = os.path.join(ROOT, "q5_lm_head_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ent[2]:
+    for f in ent[1]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     digest, traffic = None, None

@@ -3,7 +3,8 @@ bounded-wait failure path, and the DFlash verify batch.
 
 * A forward captured into a CUDA graph (batch-1 kernel, tensor-core path with
   its programmatic dependent launch, generic path, logprobs) replays to the
-  same bits as the eager call, twice in a row (the argmax workspace re-arms).
+  same bits as the eager call, twice in a row (the argmax workspace and the
+  shared-tile counters of the tensor-core path re-arm).
 * Failure detection without a GPU fault: a self-test kernel waits on an
   mbarrier that nothing arrives on; the bounded wait gives up, the status word
   records it, the kernel returns, and the context keeps working.
@@ -39,6 +40,7 @@ def _dev(torch, a):
 
 
 @pytest.mark.parametrize("n,k,b,path", [(2048, 6656, 1, "gemv_b1"), (3000, 6656, 4, "gemm_tc"),
+                                        (20000, 6656, 8, "gemm_tc"),    # tiles shared by two CTAs
                                         (500, 768, 2, "gemv_generic")])
 def test_forward_replayed_from_a_cuda_graph_matches_eager(torch_cuda, n, k, b, path):
     import q5_lm_head_gb300 as mlh
