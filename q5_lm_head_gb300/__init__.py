@@ -273,7 +273,9 @@ class LMHead:
 
     def forward_host(self, hidden_host, weights, gamma=None, eps: float = RMS_EPS, scale: float = LOGIT_SCALE,
                      cap: float = SOFTCAP, logits_host=None, argmax_host=None, stream=None):
-        """Host-memory forward: hidden_host [B, k] f32 CPU tensor (pinned for speed); returns CPU tensors."""
+        """Host-memory forward: hidden_host [B, k] f32 CPU tensor (pinned for speed); returns CPU tensors.
+        Pinned output tensors (the default) are written by the kernels directly through the
+        device's mapping of host memory; pageable ones are filled by a copy after the kernels."""
         import torch
         if hidden_host.dim() == 1:
             hidden_host = hidden_host.unsqueeze(0)
