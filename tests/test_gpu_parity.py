@@ -241,6 +241,31 @@ def test_forward_host_matches_device_forward(torch_cuda):
     assert torch.equal(ld.cpu(), lp) and torch.equal(ad.cpu(), ap) and torch.equal(ad.cpu(), ao)
 
 
+@pytest.mark.parametrize("b,path", [(4, "gemm_tc"), (1, "gemv_b1")])
+def test_forward_host_batches_and_repeats(torch_cuda, b, path):
+    """Host-buffer forwards on the batch-1 and tensor-core paths, three calls in
+    a row with changing rows: each sees its own rows and matches the device
+    forward bit for bit and the oracle within the bar."""
+    import q5_lm_head_gb300 as mlh
+    torch = torch_cuda
+    n, k = 5000, 6656
+    wq = synth.q5k_matrix(n, k, synth.stream_key(6, "W:host"), boost_rows=(17,), boost=40.0)
+    gamma = synth.normal_f64(k, synth.stream_key(6, "G:host"), 1.0, 0.1).astype(np.float32)
+    rows = [synth.normal_f64(b * k, synth.stream_key(6 + i, "H:host")).astype(np.float32).reshape(b, k)
+            for i in range(3)]
+    with mlh.LMHead(n, k, max_batch=b, device=0) as head:
+        assert head.path_name(b) == path
+        w_d, g_d = _dev(torch, wq), _dev(torch, gamma)
+        outs = [[t.clone() for t in head.forward_host(torch.from_numpy(h).pin_memory(), w_d, g_d)] for h in rows]
+        dev = [head.forward(_dev(torch, h), w_d, g_d) for h in rows]
+        torch.cuda.synchronize()
+        assert head.device_status() == 0
+    for (lh, ah), (ld, ad), h in zip(outs, dev, rows):
+        assert torch.equal(ld.cpu(), lh) and torch.equal(ad.cpu(), ah)
+        assert_parity(lh.numpy(), ah.numpy(), oracle.lmhead(h, gamma, wq, synth.LOGIT_SCALE, synth.SOFTCAP,
+                                                            synth.RMS_EPS), f"host rows b={b}")
+
+
 def test_two_handles_on_two_streams(torch_cuda):
     import q5_lm_head_gb300 as mlh
     torch = torch_cuda
