@@ -151,6 +151,35 @@ def test_random_shapes(torch_cuda, n, k, b, norm, cap, want_argmax):
 
 
 # ------------------------------------------------------------- edge cases
+def _edge_rows(k):
+    """Hidden rows at the edges of the final norm: all zero (x = 0, every logit
+    0), one spike of 1e4 over a 1e-3 floor (one activation dominates its
+    64-column group), 1e-20 scale (mean(h^2) far below eps), 1e15 scale."""
+    base = synth.normal_f64(k, synth.stream_key(11, "H:edge")).astype(np.float32)
+    spike = (base * 1e-3).astype(np.float32)
+    spike[k // 3] = 1e4
+    return np.stack([np.zeros(k, np.float32), spike, (base * 1e-20).astype(np.float32),
+                     (base * 1e15).astype(np.float32)])
+
+
+@pytest.mark.parametrize("b,path", [(1, "gemv_b1"), (4, "gemm_tc")])
+def test_edge_hidden_rows(torch_cuda, b, path):
+    import q5_lm_head_gb300 as mlh
+    n, k = 3000, 6656
+    rows = _edge_rows(k)
+    wq = synth.q5k_matrix(n, k, synth.stream_key(11, "W:edge"), boost_rows=(7,), boost=40.0)
+    gamma = synth.normal_f64(k, synth.stream_key(11, "G:edge"), 1.0, 0.1).astype(np.float32)
+    with mlh.LMHead(n, k, max_batch=b, device=0) as head:
+        assert head.path_name(b) == path
+    batches = [rows[i:i + 1] for i in range(4)] if b == 1 else [rows]
+    for hidden in batches:
+        got, am = run_case(torch_cuda, hidden, gamma, wq, n, k, synth.LOGIT_SCALE, synth.SOFTCAP, max_batch=b)
+        ref = oracle.lmhead(hidden, gamma, wq, synth.LOGIT_SCALE, synth.SOFTCAP, synth.RMS_EPS)
+        assert_parity(got, am, ref, f"edge rows on {path}")
+        if not hidden[0].any():                       # the zero row: every logit exactly 0, argmax 0
+            assert np.all(got[0] == 0.0) and int(am[0]) == 0
+
+
 def test_all_equal_logits_pick_row_zero(torch_cuda):
     n, k = 1234, 6656
     wq = np.zeros((n, k // 256 * 176), np.uint8)     # every weight is 0 -> every logit is 0
