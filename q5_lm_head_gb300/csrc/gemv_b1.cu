@@ -86,6 +86,7 @@ struct B1Cfg {
   // before when both do not fit one stage
   static_assert(NB * kBlockWeights * 4 <= kStageBytes, "hidden fits one stage");
   static constexpr int kHoldStages = 2 * NB * kBlockWeights * 4 <= kStageBytes ? 1 : 2;
+  static constexpr int kEarlyTiles = kStages - kHoldStages;   // armed before the CTA-wide barrier
   // after the activations are loaded the staging stage holds, per unit, the
   // four (amax, sum) pairs of its quarters and its plane words (p2, p1, p0:
   // 16 words each, padded to 52 so the units' rows fall on distinct banks)
@@ -271,6 +272,25 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     *s_best = 0ull;
     *s_abort = 0u;
     ptx::fence_barrier_init();
+    // The copies start here, from code this thread is already running: first
+    // the hidden row and gamma (the prologue waits on them), then the first
+    // weight tiles (the stages that hold no prologue data); the producers arm
+    // the later tiles.
+    {
+      const uint32_t row_bytes = static_cast<uint32_t>(K) * 4u;
+      ptx::mbar_arrive_expect_tx(pro_full, gamma ? 2u * row_bytes : row_bytes);
+      ptx::bulk_g2s_nohint(const_cast<float *>(s_hidden), hidden, row_bytes, pro_full);
+      if (gamma) ptx::bulk_g2s_nohint(const_cast<float *>(s_gamma), gamma, row_bytes, pro_full);
+    }
+    const uint64_t policy = ptx::policy_evict_first();
+    for (int j = 0; j < C::kEarlyTiles; ++j) {
+      const int64_t tile = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
+      if (tile >= n_tiles) break;
+      const TileLoc L = locate<kGroup>(segs, tile);
+      const uint32_t bytes = static_cast<uint32_t>(L.rows * C::kRowBytes);
+      ptx::mbar_arrive_expect_tx(&full[j], bytes);
+      ptx::bulk_g2s(stages + j * C::kStageBytes, segs.seg[L.s].w + L.r0 * C::kRowBytes, bytes, &full[j], policy);
+    }
   }
   __syncthreads();
 
@@ -286,12 +306,6 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     const int pw = warp - C::kConsumerWarps;
     const uint64_t policy = ptx::policy_evict_first();
     constexpr int kHoldTile = C::kStages - 1;  // local tile whose stage holds the prologue data
-    if (pw == (kHoldTile & 1) && lane == 0) {
-      const uint32_t row_bytes = static_cast<uint32_t>(K) * 4u;
-      ptx::mbar_arrive_expect_tx(pro_full, gamma ? 2u * row_bytes : row_bytes);
-      ptx::bulk_g2s_nohint(const_cast<float *>(s_hidden), hidden, row_bytes, pro_full);
-      if (gamma) ptx::bulk_g2s_nohint(const_cast<float *>(s_gamma), gamma, row_bytes, pro_full);
-    }
     // epilogue: lane pair (2er, 2er+1) sums row er's block partials, alternating
     static_assert(kRows <= 16, "two lanes per row");
     const int er = lane >> 1, eq = lane & 1;
@@ -345,7 +359,7 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
           break;
         }
       }
-      if (lane == 0) {
+      if (lane == 0 && j >= C::kEarlyTiles) {   // the first ones went out with the barrier set-up
         const TileLoc L = locate<kGroup>(segs, blockIdx.x + static_cast<int64_t>(j) * gridDim.x);
         const uint32_t bytes = static_cast<uint32_t>(L.rows * C::kRowBytes);
         const int st = j % C::kStages;
