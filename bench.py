@@ -13,11 +13,12 @@ cpu_baseline (the f64 oracle on this host's cores, a bounded row sample), e2e
 (the same metric through the host-buffer C-ABI call, copies included), clocks
 sampled during the timed region, gpu_launches.
 
---impl reference times the oracle (the reference implementation of this
-build) on the host cores, as it stands, on the same workload and metric.
+--impl reference times the f64 CPU oracle, as it stands, on the host cores, on
+the same workload and metric.
 
-Multi-GPU: the stage does not shard in this deployment; --gpus N runs N
-independent replicas (one per rank), value = all ranks' bytes / max time.
+Multi-GPU: each rank runs an independent replica of the output stage (no
+sharding, no collective); --gpus N runs N of them, value = all ranks' bytes /
+the slowest rank's time.
 """
 from __future__ import annotations
 

@@ -1,8 +1,8 @@
 """Multi-process host logic of the replica bench, on CPU ranks (gloo).
 
-The output stage does not shard in this deployment: `bench.py --gpus N` runs N
-independent replicas and reports every rank's bytes over the slowest rank's
-time.  These tests run that aggregation with two gloo ranks, and check that
+Each rank runs an independent replica of the output stage (no sharding, no
+collective): `bench.py --gpus N` runs N of them and reports every rank's bytes
+over the slowest rank's time.  These tests run that aggregation with two gloo ranks, and check that
 the reference arm does its work on rank 0 only.
 """
 import os
