@@ -112,6 +112,18 @@ _PROFILED = {("gemv_b1", "lmhead_b1"): ("gemv_b1_lmhead.md", _B1_SRC),
              ("gemv_b1_group", "attn_qkvg"): ("gemv_b1_group_attn_qkvg.md", _B1_SRC)}
 
 
+def kernel_code(name: str) -> str:
+    """A kernel source file's code with comments and blank lines removed, the
+    text the profile summaries' kernel-source hash covers (a comment edit does
+    not change the profiled kernel)."""
+    import re
+    with open(os.path.join(ROOT, "q5_lm_head_gb300", "csrc", name)) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def _profiled_traffic(kernel_path: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, or None when there
     is none for this kernel/workload or the kernel source changed since."""
@@ -119,11 +131,9 @@ def _profiled_traffic(kernel_path: str, workload: str):
     ent = _PROFILED.get((kernel_path, workload))
     if not ent:
         return None
-    csrc = os.path.join(ROOT, "q5_lm_head_gb300", "csrc")
     h = hashlib.sha256()
     for f in ent[1]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        h.update(kernel_code(f).encode())
     digest, traffic = None, None
     try:
         with open(os.path.join(ROOT, "profiles", ent[0])) as fh:

@@ -28,9 +28,11 @@
 //     the stage ring, so a slot is never rewritten before its producer has read
 //     it (the rewrite needs a stage that the same producer arms only
 //     afterwards).
-//   * prologue: the producer that owns the last stage first fills it with the
-//     hidden row (and gamma), one bulk copy per tensor;
-//     the consumers build the RMS factor and their activation planes from
+//   * prologue: the thread that initialises the barriers bulk-copies the
+//     hidden row (and gamma) into the last stage (gamma into the one before
+//     when both do not fit) and then arms the first weight tiles of the other
+//     stages itself, before the CTA-wide barrier; the producers arm the rest.
+//     The consumers build the RMS factor and their activation planes from
 //     shared memory (the four threads of a unit each quantise a quarter of its
 //     64 columns and share the plane words through the same stage), then
 //     release the stage, and only then is it armed with its first weight tile.

@@ -64,3 +64,16 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     args = argparse.Namespace(steps=1, warmup=0)
     assert bench.run_reference(args, synth.WORKLOADS["tiny"]) is None
     assert capsys.readouterr().out == ""                        # no line, no work on rank 1
+
+
+def test_profile_hash_ignores_comments_only():
+    """The profile summaries' kernel-source hash covers code, not comments: the
+    stripped text keeps every code line and drops comment-only and blank lines."""
+    import bench
+    code = bench.kernel_code("ptx.cuh")
+    assert "mbar_init" in code and "cp.async.bulk" in code
+    for line in code.splitlines():
+        assert line.strip() and not line.lstrip().startswith("//")
+    raw = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "q5_lm_head_gb300", "csrc", "ptx.cuh")).read()
+    assert len(code) < len(raw)
