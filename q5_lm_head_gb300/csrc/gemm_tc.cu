@@ -24,8 +24,9 @@
 //    finishes the rows.  With 32 slots the hand-off of the 32 partial columns
 //    costs more than the balance gains (measured), and tiles go round-robin.
 //    * weight producer warp: per block kb, one 2-D TMA box of 128 rows x 176
-//      bytes (144 for Q4_K) into a ring of weight stages.  Package producer warp: the kb
-//      activation package (1-D bulk copy) into a ring of package stages.
+//      bytes (144 for Q4_K) into a ring of weight stages.  Package producer
+//      warp: the kb activation package (1-D bulk copy) into a ring of package
+//      stages.
 //    * four unpack warpgroups in two pairs; pair p takes the blocks whose step
 //      index has parity p, so the two pairs work on consecutive blocks at once
 //      with their own tensor-memory buffers.  In a pair, thread r of either
