@@ -116,6 +116,34 @@ def test_bounded_wait_gives_up_and_reports_without_a_fault(torch_cuda):
     assert np.abs(logits.cpu().numpy() - ref).max() <= 2e-3
 
 
+def test_cleared_status_then_tensor_core_forward(torch_cuda):
+    """The same failure path on a handle with the tensor-core workspace: after
+    the self-test and the clear (which also re-arms the shared-tile counters), a
+    batch-4 forward over more tiles than SMs (tiles shared by two CTAs) matches
+    the oracle and records no fault."""
+    import q5_lm_head_gb300 as mlh
+    torch = torch_cuda
+    n, k, b = 20000, 6656, 4
+    wq = synth.q5k_matrix(n, k, synth.stream_key(12, "W:clear"))
+    hidden = synth.normal_f64(b * k, synth.stream_key(12, "H:clear")).astype(np.float32).reshape(b, k)
+    gamma = synth.normal_f64(k, synth.stream_key(12, "G:clear"), 1.0, 0.1).astype(np.float32)
+    with mlh.LMHead(n, k, max_batch=b, device=0) as head:
+        assert head.path_name(b) == "gemm_tc"
+        assert mlh.muse_lmhead_selftest_wait_timeout(head.handle) == 0
+        torch.cuda.synchronize()
+        assert head.device_status() & mlh.STATUS_WAIT_TIMEOUT
+        assert mlh.muse_lmhead_clear_device_status(head.handle) == 0
+        torch.cuda.synchronize()
+        assert head.device_status() == 0
+        logits, amax = head.forward(_dev(torch, hidden), _dev(torch, wq), _dev(torch, gamma))
+        torch.cuda.synchronize()
+        assert head.device_status() == 0
+    ref = oracle.lmhead(hidden, gamma, wq, synth.LOGIT_SCALE, synth.SOFTCAP, synth.RMS_EPS)
+    assert np.abs(logits.cpu().numpy() - ref).max() <= 2e-3
+    want, gap, got = oracle.argmax_first(ref), oracle.top2_gap(ref), amax.cpu().numpy()
+    assert all(int(got[i]) == int(want[i]) for i in range(b) if gap[i] > 4e-3)
+
+
 def test_dflash_verify_batch16(torch_cuda):
     import q5_lm_head_gb300 as mlh
     torch = torch_cuda
