@@ -128,13 +128,17 @@ CASES = [
     (7, 256, 3, True, 20.0, True),
     (33, 512, 2, False, 0.0, True),
     (4096, 4096, 1, True, 20.0, True),
-    (4099, 6656, 1, True, 20.0, True),      # ragged tail of the 8-row tiles
+    (4099, 6656, 1, True, 20.0, True),      # ragged tail of the 12-row tiles
     (1000, 6656, 1, False, 0.0, False),
     (4096, 6656, 5, True, 20.0, True),
     (777, 1024, 32, True, 20.0, True),
     (64, 4096, 16, True, 30.0, True),
     (19600, 1024, 4, True, 20.0, True),     # more 128-row tiles than SMs: tiles shared by two CTAs
     (57857, 1024, 3, False, 0.0, True),     # shared tiles and a one-row last tile
+    (1, 512, 2, True, 20.0, True),          # one row on the tensor-core path
+    (300, 16384, 1, True, 20.0, True),      # large K, batch 1: generic kernel
+    (300, 16384, 2, True, 20.0, True),      # large K on the tensor cores (64 blocks per row)
+    (129, 65536, 3, False, 0.0, True),      # 256 blocks per row, cap off
 ]
 
 
