@@ -82,9 +82,10 @@ int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k,
  * scales and mins, then 128 bytes of nibbles placed as in Q5_K, no high bits
  * (q in 0..15, w = d*sc*q - dmin*m); 144 bytes per 256 weights.  Every forward
  * of the handle reads its weights in this format (weights = n_rows * (k/256) *
- * 144 bytes for Q4_K).  Batch 1 with k = 4,096 or 6,656 runs the fused kernel;
- * other shapes run the generic kernel (the tensor-core path reads Q5_K only).
- * muse_lmhead_forward_group and muse_lmhead_forward_b1_noalloc read Q5_K only.
+ * 144 bytes for Q4_K).  Batch 1 with k = 4,096 or 6,656 runs the fused kernel,
+ * batches 2..32 with an even number of blocks per row the tensor-core kernel,
+ * other shapes the generic kernel, in either format.  muse_lmhead_forward_group
+ * reads the handle's format; muse_lmhead_forward_b1_noalloc reads Q5_K only.
  */
 int muse_lmhead_init_format(muse_lmhead **out, int device, int64_t n_rows, int64_t k,
                             int max_batch, int format);
@@ -243,7 +244,8 @@ typedef struct muse_gemv_segment {
  * architecture", Figure 9.1 and §9.8: Q and gate [6656 -> 4096], K and V
  * [6656 -> 256]).
  *   h         a handle; only its k (4,096 or 6,656, else MUSE_ERR_SHAPE), its
- *             device and its status word are used.
+ *             weight format (every segment's weights are in it), its device
+ *             and its status word are used.
  *   hidden    [k] f32, device, 16-byte aligned.
  *   gamma     [k] f32, device, 16-byte aligned, or NULL; eps as for forward.
  *   segments  host array of n_segments (1..MUSE_MAX_SEGMENTS) descriptions.

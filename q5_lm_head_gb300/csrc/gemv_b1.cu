@@ -610,9 +610,18 @@ cudaError_t launch_b1(const LaunchArgs &a) {
 }
 
 cudaError_t launch_b1_group(const float *hidden, const float *gamma, float eps, int k, const GemvSegment *segs,
-                            int n, uint32_t *status, int num_sms, cudaStream_t stream) {
+                            int n, uint32_t *status, int num_sms, cudaStream_t stream, bool q4) {
   if (n < 1 || n > kMaxSegments) return cudaErrorInvalidValue;
   const SegTable T = make_table(segs, n);
+  if (q4) {
+    switch (k / kBlockWeights) {
+      case 26: return launch_b1_nb<26, true, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status,
+                                                   nullptr, num_sms, stream);
+      case 16: return launch_b1_nb<16, true, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status,
+                                                   nullptr, num_sms, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (k / kBlockWeights) {
     case 26: return launch_b1_nb<26, true, false>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status,
                                                   nullptr, num_sms, stream);

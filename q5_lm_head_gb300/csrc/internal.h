@@ -59,7 +59,7 @@ bool b1_supported(int k);                            // fast batch-1 kernel comp
 cudaError_t launch_b1(const LaunchArgs &a);          // fused batch-1 kernel
 // Up to kMaxSegments matrices against one normed input row, one launch (K as for b1_supported).
 cudaError_t launch_b1_group(const float *hidden, const float *gamma, float eps, int k, const GemvSegment *segs,
-                            int n, uint32_t *status, int num_sms, cudaStream_t stream);
+                            int n, uint32_t *status, int num_sms, cudaStream_t stream, bool q4 = false);
 
 int generic_launches(const LaunchArgs &a);
 

@@ -191,7 +191,6 @@ int muse_lmhead_forward_group(muse_lmhead *h, const float *hidden, const float *
   if (!h || !hidden || !segments) return MUSE_ERR_NULL;
   if (n_segments < 1 || n_segments > MUSE_MAX_SEGMENTS) return MUSE_ERR_SHAPE;
   if (!muse::b1_supported(static_cast<int>(h->k))) return MUSE_ERR_SHAPE;
-  if (h->format != MUSE_FORMAT_Q5_K) return MUSE_ERR_VALUE;   // the grouped kernel reads Q5_K
   if (gamma && (!std::isfinite(eps) || eps < 0.0f)) return MUSE_ERR_VALUE;
   if (!aligned(hidden, 16) || (gamma && !aligned(gamma, 16))) return MUSE_ERR_ALIGN;
   muse::GemvSegment segs[muse::kMaxSegments];
@@ -206,7 +205,8 @@ int muse_lmhead_forward_group(muse_lmhead *h, const float *hidden, const float *
   DeviceGuard dg(h->device);
   if (!dg.ok) return MUSE_ERR_DEVICE;
   const cudaError_t e = muse::launch_b1_group(hidden, gamma, eps, static_cast<int>(h->k), segs, n_segments,
-                                              h->ws.status, h->num_sms, static_cast<cudaStream_t>(stream));
+                                              h->ws.status, h->num_sms, static_cast<cudaStream_t>(stream),
+                                              h->format == MUSE_FORMAT_Q4_K);
   return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
 }
 

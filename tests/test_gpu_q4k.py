@@ -5,8 +5,8 @@ LM head, and the soft cap" §20.8) against the f64 oracle's own Q4_K parser.
 Same bar as Q5_K: |gpu - oracle| <= 2e-3 on every logit, argmax equal where
 the oracle's top-2 gap exceeds 4e-3.  Covers the fused batch-1 kernel (K =
 6,656 and 4,096), the tensor-core kernel (batches 2..32, an even number of
-blocks per row), the generic kernel (the other shapes) and the logprobs
-forward.
+blocks per row), the generic kernel (the other shapes), the logprobs forward
+and the grouped batch-1 call.
 """
 import numpy as np
 import pytest
@@ -119,7 +119,7 @@ def test_q4k_logprobs(torch_cuda, b):
     assert np.abs(lp - ref_lp).max() <= TOL and np.abs(lse - ref_lse).max() <= TOL
 
 
-def test_q4k_handle_rejects_q5k_sized_weights_and_the_group_call(torch_cuda):
+def test_q4k_handle_rejects_q5k_sized_weights(torch_cuda):
     import q5_lm_head_gb300 as mlh
     torch = torch_cuda
     n, k = 64, 6656
@@ -127,7 +127,30 @@ def test_q4k_handle_rejects_q5k_sized_weights_and_the_group_call(torch_cuda):
     with mlh.LMHead(n, k, max_batch=1, device=0, fmt="q4_k") as head:
         with pytest.raises(ValueError):
             head.forward(torch.zeros((1, k), device="cuda"), w5)
-        out = torch.empty((n,), dtype=torch.float32, device="cuda")
-        st = mlh.muse_lmhead_forward_group(head.handle, torch.zeros((k,), device="cuda").data_ptr(), None, 1e-5,
-                                           [(w5.data_ptr(), n, out.data_ptr(), 1.0, 0.0)], None)
-        assert st == -5                                   # the grouped kernel reads Q5_K only
+        with pytest.raises(ValueError):
+            head.forward_group(torch.zeros((k,), device="cuda"), [(w5, n, 1.0, 0.0, None)])
+
+
+@pytest.mark.parametrize("k,shapes", [
+    (6656, ((4096, 1.0, 0.0), (4096, 1.0, 0.0), (256, 1.0, 0.0), (256, synth.LOGIT_SCALE, synth.SOFTCAP))),
+    (4096, ((6656, 1.0, 0.0), (300, 1.0, 0.0))),
+])
+def test_q4k_grouped_call(torch_cuda, k, shapes):
+    """The grouped batch-1 call on Q4_K matrices (the attention group's shapes
+    at K = 6,656; two matrices at K = 4,096), against the oracle per matrix."""
+    import q5_lm_head_gb300 as mlh
+    torch = torch_cuda
+    rng = np.random.default_rng(k)
+    hidden = rng.standard_normal(k).astype(np.float32)
+    gamma = (1.0 + 0.1 * rng.standard_normal(k)).astype(np.float32)
+    mats = [synth.q5k_matrix(n, k, synth.stream_key(13 + i, f"W:q4grp{k}"), fmt="q4_k")
+            for i, (n, _, _) in enumerate(shapes)]
+    with mlh.LMHead(max(n for n, _, _ in shapes), k, max_batch=1, device=0, fmt="q4_k") as head:
+        outs = head.forward_group(_dev(torch, hidden), [(_dev(torch, w), n, sc, cp, None)
+                                                        for w, (n, sc, cp) in zip(mats, shapes)],
+                                  _dev(torch, gamma), synth.RMS_EPS)
+        torch.cuda.synchronize()
+        assert head.device_status() == 0
+    for out, w, (n, sc, cp) in zip(outs, mats, shapes):
+        ref = oracle.lmhead(hidden.reshape(1, k), gamma, w, sc, cp, synth.RMS_EPS, fmt="q4_k")[0]
+        assert np.abs(out.cpu().numpy().astype(np.float64) - ref).max() <= TOL
