@@ -83,8 +83,9 @@ int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k,
  * (q in 0..15, w = d*sc*q - dmin*m); 144 bytes per 256 weights.  Every forward
  * of the handle reads its weights in this format (weights = n_rows * (k/256) *
  * 144 bytes for Q4_K).  Batch 1 with k = 4,096 or 6,656 runs the fused kernel,
- * batches 2..32 with an even number of blocks per row the tensor-core kernel,
- * other shapes the generic kernel, in either format.  muse_lmhead_forward_group
+ * other batches (and batch 1 at another k) with an even number of blocks per
+ * row the tensor-core kernel, other shapes the generic kernel, in either
+ * format.  muse_lmhead_forward_group
  * reads the handle's format; muse_lmhead_forward_b1_noalloc reads Q5_K only.
  */
 int muse_lmhead_init_format(muse_lmhead **out, int device, int64_t n_rows, int64_t k,

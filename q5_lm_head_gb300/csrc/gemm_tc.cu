@@ -696,11 +696,12 @@ size_t tc_split_floats(int num_sms, int max_batch) {
 
 size_t tc_split_counters(int num_sms) { return static_cast<size_t>(num_sms) * (kUnpackWarps / 2); }
 
-// Batches 2..32 with an even number of blocks per row (both pairs of unpack
-// warpgroups then own blocks of every tile), either weight format.
+// Batches 1..32 with an even number of blocks per row (both pairs of unpack
+// warpgroups then own blocks of every tile), either weight format.  Batch 1
+// takes this path only for a K the fused batch-1 kernel has no build for.
 bool tc_supported(int batch, int k) {
   const int nb = k / kBlockWeights;
-  return batch >= 2 && batch <= 32 && nb >= 2 && nb % 2 == 0;
+  return batch >= 1 && batch <= 32 && nb >= 2 && nb % 2 == 0;
 }
 
 cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_rows, int k, bool q4) {

@@ -100,6 +100,10 @@ int run_forward(muse_lmhead *h, const float *hidden, int batch, const float *gam
   switch (choose_path(h, batch)) {
     case Path::B1: e = muse::launch_b1(a); break;
     case Path::TensorCore:
+      if (!h->ws.xpkg || !h->ws.split_cnt || !h->ws.split_part) {   // never launch without its workspace
+        e = cudaErrorInvalidValue;
+        break;
+      }
       if (h->wmap_ptr != weights) {
         e = muse::tc_encode_weights(&h->wmap, weights, h->n_rows, static_cast<int>(h->k), a.q4);
         if (e != cudaSuccess) break;
@@ -154,7 +158,10 @@ int muse_lmhead_init_format(muse_lmhead **out, int device, int64_t n_rows, int64
   const size_t misc_b = 256;
   const size_t lse_b = sizeof(float2) * static_cast<size_t>(max_batch) * muse::kMaxLseParts;
   const size_t x_b = sizeof(float) * static_cast<size_t>(max_batch) * static_cast<size_t>(k);
-  const bool tc = max_batch >= 2;
+  // the tensor-core path's workspace, wherever some batch size of this handle
+  // takes that path (batch 1 does for a K without a fused batch-1 build)
+  const bool tc = muse::tc_supported(max_batch, static_cast<int>(k)) &&
+                  (max_batch >= 2 || !muse::b1_supported(static_cast<int>(k)));
   const size_t pkg_b = tc ? muse::tc_workspace_bytes(static_cast<int>(k)) : 0;
   const size_t cnt_b = tc ? (sizeof(unsigned int) * muse::tc_split_counters(h->num_sms) + 255) / 256 * 256 : 0;
   const size_t part_b = tc ? sizeof(float) * muse::tc_split_floats(h->num_sms, max_batch) : 0;

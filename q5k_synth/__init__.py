@@ -17,6 +17,7 @@ attention projections of "Chapter 9 — The Muse Glimmer architecture" §9.3):
 * ``sweep_b{1,2,4,8,16,32}``  N=202,048 x 6,656, no boosted rows
 * ``dflash_verify_b16``  B=16 (the drafted positions), rows scaled by U(0.5, 4)
 * ``lmhead_q4k_b1`` ``lmhead_q4k_b8``  the Q4_K head (756.5 MB), B=1 and B=8
+* ``ffn_up_q4k`` ``ffn_down_q4k``  one block's FFN shapes in Q4_K, B=1
 """
 from __future__ import annotations
 
@@ -252,6 +253,13 @@ WORKLOADS["dflash_verify_b16"] = _lm("dflash_verify_b16", 16, BOOSTED_ROWS, (0.5
 # the Q4_K head alternative (756.5 MB), batch 1, same shapes and boosted rows
 WORKLOADS["lmhead_q4k_b1"] = Workload("lmhead_q4k_b1", VOCAB, HIDDEN, 1, "W:lmhead_q4k", boost_rows=BOOSTED_ROWS,
                                       hidden_tag="H:lmhead_q4k_b1", fmt="q4_k")
+# the FFN of one block in Q4_K ("Chapter 9 — The Muse Glimmer architecture", Figure 9.1:
+# gate and up [6656 -> 19968], down [19968 -> 6656]); batch 1, no norm, scale 1, no cap
+FFN_WIDTH = 19968
+WORKLOADS["ffn_up_q4k"] = Workload("ffn_up_q4k", FFN_WIDTH, HIDDEN, 1, "W:ffn_up_q4k", norm=False, scale=1.0,
+                                   cap=0.0, argmax=False, hidden_tag="H:ffn_up_q4k", fmt="q4_k")
+WORKLOADS["ffn_down_q4k"] = Workload("ffn_down_q4k", HIDDEN, FFN_WIDTH, 1, "W:ffn_down_q4k", norm=False,
+                                     scale=1.0, cap=0.0, argmax=False, hidden_tag="H:ffn_down_q4k", fmt="q4_k")
 WORKLOADS["lmhead_q4k_b8"] = Workload("lmhead_q4k_b8", VOCAB, HIDDEN, 8, "W:lmhead_q4k", boost_rows=BOOSTED_ROWS,
                                       row_scale=(0.5, 4.0), hidden_tag="H:lmhead_q4k_b8", fmt="q4_k")
 

@@ -136,7 +136,8 @@ CASES = [
     (19600, 1024, 4, True, 20.0, True),     # more 128-row tiles than SMs: tiles shared by two CTAs
     (57857, 1024, 3, False, 0.0, True),     # shared tiles and a one-row last tile
     (1, 512, 2, True, 20.0, True),          # one row on the tensor-core path
-    (300, 16384, 1, True, 20.0, True),      # large K, batch 1: generic kernel
+    (300, 16384, 1, True, 20.0, True),      # large K, batch 1: tensor-core kernel (no fused build for this K)
+    (300, 16640, 1, True, 20.0, True),      # 65 blocks per row, batch 1: generic kernel
     (300, 16384, 2, True, 20.0, True),      # large K on the tensor cores (64 blocks per row)
     (129, 65536, 3, False, 0.0, True),      # 256 blocks per row, cap off
 ]

@@ -86,7 +86,8 @@ def test_q4k_full_head_batch8(torch_cuda):
     (129, 6656, 2, False, 0.0, "gemm_tc"),      # one row past a tile, cap off
     (5000, 4096, 16, True, 20.0, "gemm_tc"),
     (1000, 512, 32, True, 20.0, "gemm_tc"),     # two blocks per row, 32 batch rows
-    (500, 512, 1, True, 20.0, "gemv_generic"),  # K with no fused kernel
+    (500, 512, 1, True, 20.0, "gemm_tc"),       # batch 1 at a K with no fused build
+    (300, 768, 1, True, 20.0, "gemv_generic"),  # batch 1, odd number of blocks per row
     (64, 768, 8, False, 0.0, "gemv_generic"),   # odd number of blocks per row
 ])
 def test_q4k_shapes(torch_cuda, n, k, b, norm, cap, path):
@@ -154,3 +155,14 @@ def test_q4k_grouped_call(torch_cuda, k, shapes):
     for out, w, (n, sc, cp) in zip(outs, mats, shapes):
         ref = oracle.lmhead(hidden.reshape(1, k), gamma, w, sc, cp, synth.RMS_EPS, fmt="q4_k")[0]
         assert np.abs(out.cpu().numpy().astype(np.float64) - ref).max() <= TOL
+
+
+@pytest.mark.parametrize("name,path", [("ffn_up_q4k", "gemv_b1"), ("ffn_down_q4k", "gemm_tc")])
+def test_q4k_ffn_shapes(torch_cuda, name, path):
+    """One block's FFN shapes in Q4_K at batch 1: gate/up [6656 -> 19968] on the
+    fused kernel, down [19968 -> 6656] (78 blocks per row, no fused build) on the
+    tensor-core kernel with one batch row."""
+    wl = synth.WORKLOADS[name]
+    hidden, gamma, wq = synth.inputs_for(wl)
+    got, _ = _run(torch_cuda, hidden, gamma, wq, wl.n_rows, wl.k, wl.scale, wl.cap, path, want_argmax=False)
+    _check(got, None, oracle.lmhead(hidden, gamma, wq, wl.scale, wl.cap, synth.RMS_EPS, fmt="q4_k"))
