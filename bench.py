@@ -106,9 +106,11 @@ class ClockSampler:
 # ncu summaries that carry a per-launch DRAM traffic figure:
 # (kernel path, workload) -> (file, kernel sources)
 _B1_SRC = ("gemv_b1.cu", "common.cuh", "ptx.cuh")
+_TC_SRC = ("gemm_tc.cu", "common.cuh", "ptx.cuh", "tc.cuh")
 _PROFILED = {("gemv_b1", "lmhead_b1"): ("gemv_b1_lmhead.md", _B1_SRC),
              ("gemv_b1", "lmhead_q4k_b1"): ("gemv_b1_lmhead_q4k.md", _B1_SRC),
-             ("gemm_tc", "lmhead_b8"): ("gemm_tc_lmhead_b8.md", ("gemm_tc.cu", "common.cuh", "ptx.cuh", "tc.cuh")),
+             ("gemm_tc", "lmhead_b8"): ("gemm_tc_lmhead_b8.md", _TC_SRC),
+             ("gemm_tc", "ffn_down_q4k"): ("gemm_tc_ffn_down_q4k.md", _TC_SRC),
              ("gemv_b1_group", "attn_qkvg"): ("gemv_b1_group_attn_qkvg.md", _B1_SRC)}
 
 

@@ -23,6 +23,11 @@
 //    and count in; the second to arrive adds the two (in a fixed order) and
 //    finishes the rows.  With 32 slots the hand-off of the 32 partial columns
 //    costs more than the balance gains (measured), and tiles go round-robin.
+//    A narrow matrix (fewer 128-row tiles than SMs) runs a separate instance
+//    (kNarrow) that deals the steps over up to one CTA per SM at any batch:
+//    a tile is then shared by all the CTAs whose ranges meet it, each leaves
+//    its sums in its slot and counts in on the tile's counter, and the last
+//    to arrive adds the slots in CTA order and finishes the rows.
 //    * weight producer warp: per block kb, one 2-D TMA box of 128 rows x 176
 //      bytes (144 for Q4_K) into a ring of weight stages.  Package producer
 //      warp: the kb activation package (1-D bulk copy) into a ring of package
@@ -286,7 +291,7 @@ __device__ __forceinline__ void ld_x4(uint32_t ta, uint32_t (&v)[4]) {
 }
 
 // ------------------------------------------------------------------ main kernel
-template <int NM, bool kQ4>
+template <int NM, bool kQ4, bool kNarrow>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const uint8_t *__restrict__ pkgs, int nb,
                    int64_t n_rows, int batch, float scale, float cap, float *__restrict__ logits,
@@ -316,11 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // keep their parity across tiles).  With at most n_tiles CTAs a share is at
   // least nb steps, so a tile is cut at most once and shared by at most two
   // CTAs.  Round-robin: tiles blockIdx.x + j * gridDim.x, none shared.
-  constexpr bool kBalanced = NM <= 16;
+  // Narrow instance: gridDim.x <= pairs, so no share is empty and the CTAs
+  // meeting a tile are consecutive; a range may lie inside one tile.
+  constexpr bool kBalanced = kNarrow || NM <= 16;
+  const int64_t pairs = n_tiles * (nb / 2);
   int64_t total, tile_first, tile_last = -1, tile_step = 1;
   int kb_first = 0, kb_end = 0;                                   // kb_end 0: the range ends on a tile boundary
   if constexpr (kBalanced) {
-    const int64_t pairs = n_tiles * (nb / 2);
     const int64_t s_begin = 2 * (pairs * blockIdx.x / gridDim.x);
     const int64_t s_end = 2 * (pairs * (blockIdx.x + 1) / gridDim.x);
     total = s_end - s_begin;
@@ -487,12 +494,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the boundary's slot, warp by warp (32 rows): both CTAs' warps store
     // their sums, then count in with one atomic per warp; the second adds
     // side 0 + side 1 (the same order in either CTA) and finishes the rows.
+    // Narrow instance: each CTA stores to its own slot (side 0 its first
+    // tile, 1 its last) and counts in on the tile's counter; the last of the
+    // sharing CTAs adds their slots in CTA order.
     uint32_t n_fin = 0;
     auto finish_tile = [&](int64_t t) -> bool {
       const int64_t row = t * kTileRows + r;
       int side = -1;
       uint32_t slot = 0;
-      if (t == tile_first && kb_first != 0) {
+      if constexpr (kNarrow) {                  // slot (blockIdx.x, 0) for the first tile, 1 for the last
+        if (t == tile_first && (kb_first != 0 || (tile_first == tile_last && kb_end != 0))) side = 0;
+        else if (t == tile_last && kb_end != 0) side = 1;
+      } else if (t == tile_first && kb_first != 0) {
         side = 1;
         slot = blockIdx.x - 1;
       } else if (t == tile_last && kb_end != 0) {
@@ -517,7 +530,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int b = 0; b < HB; ++b) v[b] = acc[b] + xw[b];
           ptx::mbar_arrive(xch_empty);
         }
-        if (ok && side >= 0) {
+        if (kNarrow && ok && side >= 0) {
+          // the CTAs c_lo..c_hi share t: owner of the tile's first and last step pair
+          const int64_t c_lo = ((t * (nb / 2) + 1) * gridDim.x - 1) / pairs;
+          const int64_t c_hi = (((t + 1) * (nb / 2)) * gridDim.x - 1) / pairs;
+          const uint32_t last = static_cast<uint32_t>(c_hi - c_lo);
+          float *mine = split_part + ((static_cast<size_t>(blockIdx.x) * 2 + side) * kTileRows + r) * NM + b0;
+#pragma unroll
+          for (int b = 0; b < HB; ++b) mine[b] = v[b];
+          __threadfence();                       // this lane's sums before the warp's count
+          __syncwarp();
+          uint32_t who = 0u;
+          unsigned int *cnt = split_cnt + t * (kUnpackWarps / 2) + (warp & 7);
+          if (lane == 0) {
+            who = atomicAdd(cnt, 1u);
+            if (who == last) *cnt = 0u;          // every sharing CTA counted in: re-armed for the next launch
+          }
+          store = __shfl_sync(0xffffffffu, who, 0) == last;
+          if (store) {
+            __threadfence();                     // the other CTAs' sums after their counts
+#pragma unroll
+            for (int b = 0; b < HB; ++b) v[b] = 0.0f;
+            for (int64_t c = c_lo; c <= c_hi; ++c) {
+              const int64_t cs = (2 * (pairs * c / gridDim.x)) / nb == t ? 0 : 1;   // t is c's first tile?
+              const float *src = split_part + ((static_cast<size_t>(c) * 2 + cs) * kTileRows + r) * NM + b0;
+#pragma unroll
+              for (int b = 0; b < HB; ++b) v[b] += __ldcg(src + b);
+            }
+          }
+        } else if (ok && side >= 0) {
           float *base = split_part + (static_cast<size_t>(slot) * 2 * kTileRows + r) * NM + b0;
           float *mine = base + side * kTileRows * NM;
 #pragma unroll
@@ -648,7 +689,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
-template <int NM, bool kQ4>
+template <int NM, bool kQ4, bool kNarrow>
 cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
   using C = TcCfg<NM, kQ4>;
   static unsigned long long configured = 0;
@@ -657,7 +698,7 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured & bit)) {
-    e = cudaFuncSetAttribute(gemm_tc_kernel<NM, kQ4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gemm_tc_kernel<NM, kQ4, kNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured |= bit;
@@ -668,7 +709,8 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t n_tiles = (a.n_rows + kTileRows - 1) / kTileRows;
-  const int64_t grid = n_tiles < a.num_sms ? n_tiles : a.num_sms;
+  const int64_t pairs = n_tiles * (nb / 2);   // a narrow matrix spreads its step pairs over the SMs
+  const int64_t grid = kNarrow ? (pairs < a.num_sms ? pairs : a.num_sms) : (n_tiles < a.num_sms ? n_tiles : a.num_sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
@@ -679,7 +721,7 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NM, kQ4>, map, static_cast<const uint8_t *>(a.ws.xpkg), nb,
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NM, kQ4, kNarrow>, map, static_cast<const uint8_t *>(a.ws.xpkg), nb,
                             a.n_rows, a.batch, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax,
                             a.ws.status, a.ws.split_part, a.ws.split_cnt);
 }
@@ -694,6 +736,8 @@ size_t tc_split_floats(int num_sms, int max_batch) {
   return static_cast<size_t>(num_sms) * 2 * kTileRows * tc_batch_slots(max_batch);
 }
 
+// per boundary between CTAs (one per SM) for a large matrix, per 128-row tile
+// for a narrow one (fewer tiles than SMs): at most max(SMs, tiles) entries
 size_t tc_split_counters(int num_sms) { return static_cast<size_t>(num_sms) * (kUnpackWarps / 2); }
 
 // Batches 1..32 with an even number of blocks per row (both pairs of unpack
@@ -721,16 +765,22 @@ cudaError_t tc_encode_weights(CUtensorMap *map, const void *weights, int64_t n_r
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_tc(const LaunchArgs &a, const CUtensorMap &map) {
+template <bool kNarrow>
+cudaError_t launch_tc_sched(const LaunchArgs &a, const CUtensorMap &map) {
   const int nm = tc_batch_slots(a.batch);
   if (a.q4) {
-    if (nm == 8) return launch_tc_nm<8, true>(a, map);
-    if (nm == 16) return launch_tc_nm<16, true>(a, map);
-    return launch_tc_nm<32, true>(a, map);
+    if (nm == 8) return launch_tc_nm<8, true, kNarrow>(a, map);
+    if (nm == 16) return launch_tc_nm<16, true, kNarrow>(a, map);
+    return launch_tc_nm<32, true, kNarrow>(a, map);
   }
-  if (nm == 8) return launch_tc_nm<8, false>(a, map);
-  if (nm == 16) return launch_tc_nm<16, false>(a, map);
-  return launch_tc_nm<32, false>(a, map);
+  if (nm == 8) return launch_tc_nm<8, false, kNarrow>(a, map);
+  if (nm == 16) return launch_tc_nm<16, false, kNarrow>(a, map);
+  return launch_tc_nm<32, false, kNarrow>(a, map);
+}
+
+cudaError_t launch_tc(const LaunchArgs &a, const CUtensorMap &map) {
+  const int64_t n_tiles = (a.n_rows + kTileRows - 1) / kTileRows;
+  return n_tiles < a.num_sms ? launch_tc_sched<true>(a, map) : launch_tc_sched<false>(a, map);
 }
 
 }  // namespace muse

@@ -20,7 +20,7 @@ struct Workspace {
   uint8_t *xpkg;             // per-block activation packages (tensor-core path)
   float2 *lse_parts;         // [MUSE_MAX_BATCH][kMaxLseParts] (max, sum exp) partials of the logprobs
   float *split_part;         // tensor-core path: [num_sms][2][128][slots] partial sums of shared tiles
-  unsigned int *split_cnt;   // [num_sms][8] arrivals per shared tile and warp, zero between forwards
+  unsigned int *split_cnt;   // [num_sms][8] arrivals per shared tile and warp (per CTA boundary, or per tile when tiles < SMs), zero between forwards
 };
 
 constexpr int kMaxLseParts = 256;

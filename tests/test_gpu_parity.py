@@ -225,15 +225,20 @@ def test_repeat_calls_are_deterministic_and_rearm_argmax(torch_cuda):
     assert_parity(l2.cpu().numpy(), a2.cpu().numpy(), ref2, "second input")
 
 
-def test_tensor_core_shared_tiles_repeat_bit_for_bit(torch_cuda):
-    """More tiles than SMs: CTAs share the tiles at their range boundaries and the
-    second to arrive finishes them.  Whichever CTA that is, the two partial sums
-    are added in a fixed order, and the arrival counters re-arm for the next call,
-    so repeated forwards (alternating inputs) give the same bits."""
+@pytest.mark.parametrize("n,k,b", [
+    (40000, 6656, 5),     # more tiles than SMs: a tile cut by a range boundary, shared by two CTAs
+    (1000, 6656, 8),      # 8 tiles over 104 CTAs: each tile shared by 13
+    (300, 16384, 20),     # 32 batch slots, 3 tiles over 96 CTAs
+    (257, 65536, 2),      # 3 tiles over every SM, one CTA range across a tile boundary, a one-row last tile
+])
+def test_tensor_core_shared_tiles_repeat_bit_for_bit(torch_cuda, n, k, b):
+    """CTAs share the tiles at their range boundaries and the last to arrive
+    finishes them.  Whichever CTA that is, the partial sums are added in a fixed
+    order, and the arrival counters re-arm for the next call, so repeated
+    forwards (alternating inputs) give the same bits."""
     import q5_lm_head_gb300 as mlh
     torch = torch_cuda
-    n, k, b = 40000, 6656, 5
-    wq = synth.q5k_matrix(n, k, synth.stream_key(2, "W:shared"), boost_rows=(777,), boost=40.0)
+    wq = synth.q5k_matrix(n, k, synth.stream_key(2, "W:shared"), boost_rows=(n // 3,), boost=40.0)
     hidden = synth.normal_f64(b * k, synth.stream_key(2, "H:shared")).astype(np.float32).reshape(b, k)
     gamma = synth.normal_f64(k, synth.stream_key(2, "G:shared"), 1.0, 0.1).astype(np.float32)
     with mlh.LMHead(n, k, max_batch=b, device=0) as head:
@@ -247,7 +252,7 @@ def test_tensor_core_shared_tiles_repeat_bit_for_bit(torch_cuda):
         assert torch.equal(outs[0][0], outs[i][0]) and torch.equal(outs[0][1], outs[i][1])
     assert torch.equal(outs[1][0], outs[3][0])
     ref = oracle.lmhead(hidden, gamma, wq, synth.LOGIT_SCALE, synth.SOFTCAP, synth.RMS_EPS)
-    assert_parity(outs[0][0].cpu().numpy(), outs[0][1].cpu().numpy(), ref, "shared tiles")
+    assert_parity(outs[0][0].cpu().numpy(), outs[0][1].cpu().numpy(), ref, f"shared tiles n={n} k={k} b={b}")
 
 
 def test_forward_host_matches_device_forward(torch_cuda):
