@@ -110,7 +110,7 @@ _TC_SRC = ("gemm_tc.cu", "common.cuh", "ptx.cuh", "tc.cuh")
 _PROFILED = {("gemv_b1", "lmhead_b1"): ("gemv_b1_lmhead.md", _B1_SRC),
              ("gemv_b1", "lmhead_q4k_b1"): ("gemv_b1_lmhead_q4k.md", _B1_SRC),
              ("gemm_tc", "lmhead_b8"): ("gemm_tc_lmhead_b8.md", _TC_SRC),
-             ("gemm_tc", "ffn_down_q4k"): ("gemm_tc_ffn_down_q4k.md", _TC_SRC),
+             ("gemv_b1_split", "ffn_down_q4k"): ("gemv_b1_split_ffn_down_q4k.md", _B1_SRC),
              ("gemv_b1_group", "attn_qkvg"): ("gemv_b1_group_attn_qkvg.md", _B1_SRC)}
 
 
@@ -412,7 +412,7 @@ def run_ours(args, wl):
         amax = torch.empty((wl.batch,), dtype=torch.int32, device=dev) if wl.argmax else None
         path, launches = head.path_name(wl.batch), head.launches_per_forward(wl.batch, wl.norm)
         if args.logprobs:           # + the apply kernel (+ a pass over the logits off the fused path)
-            launches += 1 if path == "gemv_b1" else 2
+            launches += 1 if path in ("gemv_b1", "gemv_b1_split") else 2
             path = path + "+logprobs"
             lse_d = torch.empty((wl.batch,), dtype=torch.float32, device=dev)
     h_d = torch.from_numpy(hidden).to(dev)

@@ -82,7 +82,10 @@ int muse_lmhead_init(muse_lmhead **out, int device, int64_t n_rows, int64_t k,
  * scales and mins, then 128 bytes of nibbles placed as in Q5_K, no high bits
  * (q in 0..15, w = d*sc*q - dmin*m); 144 bytes per 256 weights.  Every forward
  * of the handle reads its weights in this format (weights = n_rows * (k/256) *
- * 144 bytes for Q4_K).  Batch 1 with k = 4,096 or 6,656 runs the fused kernel,
+ * 144 bytes for Q4_K).  Batch 1 with k = 4,096 or 6,656 runs the fused kernel;
+ * batch 1 with k = S x 6,656 or S x 4,096 (S = 2..16, n_rows * S at most 2^26)
+ * runs the same kernel split along k into S column chunks (the workspace then
+ * holds n_rows * S floats of chunk partial sums and one counter per 12 rows);
  * other batches (and batch 1 at another k) with an even number of blocks per
  * row the tensor-core kernel, other shapes the generic kernel, in either
  * format.  muse_lmhead_forward_group
@@ -120,7 +123,7 @@ int muse_lmhead_forward(muse_lmhead *h, const float *hidden, int batch,
  *   lse      [batch] f32, device, 4-byte aligned, written; or NULL to skip it.
  *   argmax   as for muse_lmhead_forward (the largest logprob's index).
  * Other arguments and validation as for muse_lmhead_forward.  At batch 1 with
- * the fused kernel the normaliser is accumulated in the kernel's epilogue and
+ * the fused kernel (k = 4,096 or 6,656) the normaliser is accumulated in the kernel's epilogue and
  * one more small launch subtracts it; other paths add a pass over the logits.
  */
 int muse_lmhead_forward_logprobs(muse_lmhead *h, const float *hidden, int batch,
@@ -155,7 +158,8 @@ int muse_lmhead_launches_per_forward(const muse_lmhead *h, int batch, int with_n
 
 /*
  * Name of the kernel path a forward with this batch size takes ("gemv_b1",
- * "gemv_generic", ...), or NULL for an invalid handle/batch.  Host-only query;
+ * "gemv_b1_split", "gemm_tc" or "gemv_generic"), or NULL for an invalid
+ * handle/batch.  Host-only query;
  * the string is static.
  */
 const char *muse_lmhead_path_name(const muse_lmhead *h, int batch);
@@ -171,8 +175,9 @@ int muse_lmhead_device_status(muse_lmhead *h, uint32_t *status_out);
 /*
  * Clear the handle's status word (asynchronous memsets on `stream`), for
  * example after a recorded timeout, once the caller has dealt with it.  Also
- * re-arms the tensor-core path's per-boundary arrival counters, which a
- * forward that gave up may have left counted in.
+ * re-arms the tensor-core path's per-boundary arrival counters and the
+ * split-K batch-1 path's per-tile chunk counters, which a forward that gave up
+ * may have left counted in.
  */
 int muse_lmhead_clear_device_status(muse_lmhead *h, void *stream);
 

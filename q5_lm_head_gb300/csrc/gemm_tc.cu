@@ -52,6 +52,7 @@
 //      accumulation into D (M = 128, N = 2*NM: the x_hi and x_lo rows side by
 //      side) and one MMA A_min x x_min into Dmin; tcgen05.commit hands the
 //      buffer back.
+#include <atomic>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -676,32 +677,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
+// The driver's tensor-map encoder, looked up once (a function-local static is
+// initialised once even when host threads race to the first call).
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     cudaDriverEntryPointQueryResult q;
     void *p = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
 template <int NM, bool kQ4, bool kNarrow>
 cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
   using C = TcCfg<NM, kQ4>;
-  static unsigned long long configured = 0;
+  static std::atomic<unsigned long long> configured{0};   // one bit per device; host threads may race here
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
-  if (!(configured & bit)) {
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(gemm_tc_kernel<NM, kQ4, kNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured |= bit;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   const int nb = a.k / kBlockWeights;
   prep_x_kernel<NM><<<dim3(nb, min_rows<NM>()), kPrepThreads, 0, a.stream>>>(a.hidden, a.gamma, a.eps, a.batch,

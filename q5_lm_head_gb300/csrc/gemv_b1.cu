@@ -9,6 +9,16 @@
 // matrices form one sequence, each tile belongs to one matrix and writes that
 // matrix's output with its own scale and cap.
 //
+// A K that is S times a built width (S x 6,656 or S x 4,096 columns) runs the
+// same kernel split along K: CTAs [c*G/S, (c+1)*G/S) of a G-CTA grid stream
+// column chunk c of every row, with chunk c of the input row.  A row tile's S
+// chunk partials meet in global memory: each chunk CTA stores its rows' sums
+// as it goes; after its last tile the CTA counts in on each of its tiles'
+// counters (a thread per tile: release fence, atomic add, acquire fence when
+// last), and the whole CTA finishes the tiles it arrived last on: the S partials added in chunk order
+// (the same bits whichever CTA that is), then scale, cap and argmax.  No CTA
+// waits on another.
+//
 // Warp roles (one CTA per SM)
 //   * consumer warps: thread (kb, c) owns 64 columns, block kb, sub-blocks 2c
 //     and 2c+1, for the whole launch (column-stationary).  Four teams of such
@@ -47,6 +57,7 @@
 //   Then raw += d * sigma * sum_s sc_s * (that) - dmin * sum_s m_s * sum_j x_j,
 //   which is sum_j (d*sc_s*q_j - dmin*m_s) x_j up to rounding (§20.1 matvec
 //   with the Q5_K weight w = d*sc*q - dmin*m).
+#include <atomic>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -235,13 +246,15 @@ __device__ __forceinline__ TileLoc locate(const SegTable &T, int64_t tile) {
   return L;
 }
 
-template <int NB, bool kGroup, bool kQ4>
+template <int NB, bool kGroup, bool kQ4, bool kSplit>
 __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     gemv_b1_kernel(const float *__restrict__ hidden, const float *__restrict__ gamma, float eps,
                    const __grid_constant__ SegTable segs, unsigned long long *keys, unsigned int *ticket,
-                   int32_t *argmax, uint32_t *status, float2 *lse_parts) {
+                   int32_t *argmax, uint32_t *status, float2 *lse_parts, int n_chunks, float *split_part,
+                   unsigned int *split_cnt) {
+  static_assert(!(kSplit && kGroup), "a grouped launch is not split along K");
   using C = B1Cfg<NB, kQ4>;
-  constexpr int K = NB * kBlockWeights;
+  constexpr int K = NB * kBlockWeights;                                    // columns of one chunk
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *stages = smem;
   float *slots = reinterpret_cast<float *>(smem + C::kStages * C::kStageBytes);
@@ -263,6 +276,37 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int64_t n_tiles = segs.tile_end[segs.n - 1];
+  // This CTA's tiles: tile_first, tile_first + tile_step, ... of its chunk
+  // (one chunk, all CTAs, unless split along K).
+  int chunk = 0;
+  int64_t tile_first = blockIdx.x, tile_step = gridDim.x;
+  if constexpr (kSplit) {
+    chunk = static_cast<int>(((static_cast<int64_t>(blockIdx.x) + 1) * n_chunks - 1) / gridDim.x);
+    const int64_t lo = static_cast<int64_t>(chunk) * gridDim.x / n_chunks;
+    tile_first = blockIdx.x - lo;
+    tile_step = (static_cast<int64_t>(chunk) + 1) * gridDim.x / n_chunks - lo;
+  }
+  const int my_tiles = tile_first < n_tiles ? static_cast<int>((n_tiles - 1 - tile_first) / tile_step) + 1 : 0;
+  // weight tiles armed by the barrier thread before the CTA-wide barrier; a
+  // split chunk's tiles are row-strided (one copy per row), so its producers
+  // arm them all, a row per lane
+  constexpr int kEarly = kSplit ? 0 : C::kEarlyTiles;
+  const float *x_src = hidden + static_cast<size_t>(chunk) * K;           // the chunk's input columns
+  const float *g_src = gamma ? gamma + static_cast<size_t>(chunk) * K : nullptr;
+  // the rows of local tile j: one bulk copy, or one per row of a split chunk
+  // (rows n_chunks * kRowBytes apart); lanes l0, l0 + ls, ... issue them
+  auto issue_tile = [&](const TileLoc &L, int st, uint64_t policy, int l0, int ls) {
+    uint8_t *dst = stages + st * C::kStageBytes;
+    if constexpr (kSplit) {
+      const int64_t stride = static_cast<int64_t>(n_chunks) * C::kRowBytes;
+      const uint8_t *src = segs.seg[0].w + L.r0 * stride + static_cast<int64_t>(chunk) * C::kRowBytes;
+      for (int i = l0; i < L.rows; i += ls)
+        ptx::bulk_g2s(dst + i * C::kRowBytes, src + i * stride, C::kRowBytes, &full[st], policy);
+    } else if (l0 == 0) {
+      ptx::bulk_g2s(dst, segs.seg[L.s].w + L.r0 * C::kRowBytes, static_cast<uint32_t>(L.rows * C::kRowBytes),
+                    &full[st], policy);
+    }
+  };
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -281,17 +325,16 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     {
       const uint32_t row_bytes = static_cast<uint32_t>(K) * 4u;
       ptx::mbar_arrive_expect_tx(pro_full, gamma ? 2u * row_bytes : row_bytes);
-      ptx::bulk_g2s_nohint(const_cast<float *>(s_hidden), hidden, row_bytes, pro_full);
-      if (gamma) ptx::bulk_g2s_nohint(const_cast<float *>(s_gamma), gamma, row_bytes, pro_full);
+      ptx::bulk_g2s_nohint(const_cast<float *>(s_hidden), x_src, row_bytes, pro_full);
+      if (gamma) ptx::bulk_g2s_nohint(const_cast<float *>(s_gamma), g_src, row_bytes, pro_full);
     }
     const uint64_t policy = ptx::policy_evict_first();
-    for (int j = 0; j < C::kEarlyTiles; ++j) {
-      const int64_t tile = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
+    for (int j = 0; j < kEarly; ++j) {
+      const int64_t tile = tile_first + static_cast<int64_t>(j) * tile_step;
       if (tile >= n_tiles) break;
       const TileLoc L = locate<kGroup>(segs, tile);
-      const uint32_t bytes = static_cast<uint32_t>(L.rows * C::kRowBytes);
-      ptx::mbar_arrive_expect_tx(&full[j], bytes);
-      ptx::bulk_g2s(stages + j * C::kStageBytes, segs.seg[L.s].w + L.r0 * C::kRowBytes, bytes, &full[j], policy);
+      ptx::mbar_arrive_expect_tx(&full[j], static_cast<uint32_t>(L.rows * C::kRowBytes));
+      issue_tile(L, j, policy, 0, 1);
     }
   }
   __syncthreads();
@@ -315,7 +358,8 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     MaxSum ms = ms_empty();                     // log-softmax normaliser of this lane's rows
     // finish the rows of local tile j (its consumers have released its stage)
     auto finish = [&](int j) {
-      const TileLoc L = locate<kGroup>(segs, blockIdx.x + static_cast<int64_t>(j) * gridDim.x);
+      const int64_t tile = tile_first + static_cast<int64_t>(j) * tile_step;
+      const TileLoc L = locate<kGroup>(segs, tile);
       const GemvSegment &G = segs.seg[L.s];
       const float *pr = slots + (j % C::kSlots) * (C::kSlotBytes / 4) + er * NB;
       float sacc = 0.0f;
@@ -325,6 +369,13 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
           if (g + eq < NB) sacc += pr[g + eq];
       }
       sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
+      if constexpr (kSplit) {
+        // this chunk's row sums out (plain stores); the CTA counts the tile in
+        // and finishes it after its last tile, off the copy-issue path
+        if (eq == 0 && er < L.rows) split_part[static_cast<int64_t>(chunk) * G.n_rows + L.r0 + er] = sacc;
+        __syncwarp();
+        return;
+      }
       if (eq == 0 && er < L.rows) {
         const int64_t row = L.r0 + er;
         const float out = scale_softcap(sacc, G.scale, G.cap);
@@ -341,7 +392,6 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
       if (lane == 0) ok = ptx::mbar_wait(&empty[j % C::kStages], static_cast<uint32_t>((j / C::kStages) & 1));
       return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     };
-    const int my_tiles = blockIdx.x < n_tiles ? static_cast<int>((n_tiles - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
     int issued = pw;                           // next local tile of this producer
     bool aborted = false;
     for (; issued < my_tiles; issued += 2) {
@@ -361,7 +411,13 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
           break;
         }
       }
-      if (lane == 0 && j >= C::kEarlyTiles) {   // the first ones went out with the barrier set-up
+      if constexpr (kSplit) {                  // every tile, one row per lane
+        const TileLoc L = locate<kGroup>(segs, tile_first + static_cast<int64_t>(j) * tile_step);
+        const int st = j % C::kStages;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(L.rows * C::kRowBytes));
+        __syncwarp();
+        issue_tile(L, st, policy, lane, 32);
+      } else if (lane == 0 && j >= C::kEarlyTiles) {   // the first ones went out with the barrier set-up
         const TileLoc L = locate<kGroup>(segs, blockIdx.x + static_cast<int64_t>(j) * gridDim.x);
         const uint32_t bytes = static_cast<uint32_t>(L.rows * C::kRowBytes);
         const int st = j % C::kStages;
@@ -406,19 +462,30 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     float r = 1.0f;
     if (gamma) {
       float ss = 0.0f;
-      for (int j = tid * 4; j < K; j += C::kConsumers * 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(s_hidden + j);
-        ss = fmaf(v.x, v.x, ss);
-        ss = fmaf(v.y, v.y, ss);
-        ss = fmaf(v.z, v.z, ss);
-        ss = fmaf(v.w, v.w, ss);
+      if constexpr (kSplit) {                   // the whole row's mean square (all chunks), from global memory
+        const int kt = K * n_chunks;
+        for (int j = tid * 4; j < kt; j += C::kConsumers * 4) {
+          const float4 v = __ldg(reinterpret_cast<const float4 *>(hidden + j));
+          ss = fmaf(v.x, v.x, ss);
+          ss = fmaf(v.y, v.y, ss);
+          ss = fmaf(v.z, v.z, ss);
+          ss = fmaf(v.w, v.w, ss);
+        }
+      } else {
+        for (int j = tid * 4; j < K; j += C::kConsumers * 4) {
+          const float4 v = *reinterpret_cast<const float4 *>(s_hidden + j);
+          ss = fmaf(v.x, v.x, ss);
+          ss = fmaf(v.y, v.y, ss);
+          ss = fmaf(v.z, v.z, ss);
+          ss = fmaf(v.w, v.w, ss);
+        }
       }
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       if (lane == 0) s_red[warp] = ss;
       ptx::named_bar_sync(1, C::kConsumers);
       float tot = 0.0f;
       for (int i = 0; i < C::kConsumerWarps; ++i) tot += s_red[i];
-      r = 1.0f / sqrtf(tot / static_cast<float>(K) + eps);
+      r = 1.0f / sqrtf(tot / static_cast<float>(kSplit ? K * n_chunks : K) + eps);
     }
     // This thread's activations: unit u = (kb, c) covers 64 columns, sub-block
     // 2c (x_lo, natural chunks 0..7 of four columns) and 2c+1 (x_hi, chunks
@@ -498,7 +565,7 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
 
     int st = 0, ps = 0;
     uint32_t ph = 0;                           // round parity of the stage ring
-    for (int64_t tile = blockIdx.x; tile < n_tiles && pro_ok; tile += gridDim.x) {
+    for (int64_t tile = tile_first; tile < n_tiles && pro_ok; tile += tile_step) {
       // every exit decision is taken by the whole warp (the loop body shuffles)
       if (__any_sync(0xffffffffu, *s_abort != 0u)) break;
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full[st], ph))) {
@@ -537,6 +604,64 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
   }
 
   __syncthreads();
+  if constexpr (kSplit) {
+    // Count this CTA's tiles in, a thread per tile; the tiles it arrived last on
+    // are finished by the whole CTA, a (tile, row) job per thread: the chunk
+    // partials added in chunk order, then scale, cap, store and argmax key.
+    if (*s_abort == 0u) {
+      int *s_list = reinterpret_cast<int *>(stages);                 // every stage is free again
+      unsigned int *s_nlast = reinterpret_cast<unsigned int *>(s_red);
+      const GemvSegment &G = segs.seg[0];
+      unsigned long long best = 0ull;
+      for (int base = 0; base < my_tiles; base += C::kThreads) {
+        if (tid == 0) *s_nlast = 0u;
+        __syncthreads();
+        const int j = base + tid;
+        if (j < my_tiles) {
+          const int64_t tile = tile_first + static_cast<int64_t>(j) * tile_step;
+          ptx::fence_acq_rel_gpu();            // release: the CTA's partial stores (seen through the barrier)
+          if (atomicAdd(split_cnt + tile, 1u) == static_cast<uint32_t>(n_chunks - 1)) {
+            split_cnt[tile] = 0u;              // every chunk counted in: re-armed for the next launch
+            ptx::fence_acq_rel_gpu();          // acquire: the other chunks' partials, for the CTA after the barrier
+            s_list[atomicAdd(s_nlast, 1u)] = j;
+          }
+        }
+        __syncthreads();
+        const int n_jobs = static_cast<int>(*s_nlast) * kRows;
+        for (int job0 = tid; job0 < n_jobs; job0 += 4 * C::kThreads) {
+          float acc[4];
+          int64_t row[4];
+          bool ok[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int job = job0 + i * C::kThreads;
+            ok[i] = job < n_jobs;
+            const TileLoc L = locate<kGroup>(segs, tile_first + static_cast<int64_t>(ok[i] ? s_list[job / kRows] : 0) * tile_step);
+            ok[i] = ok[i] && job % kRows < L.rows;
+            row[i] = L.r0 + job % kRows;
+            acc[i] = 0.0f;
+          }
+          for (int q = 0; q < n_chunks; ++q) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (ok[i]) acc[i] += __ldcg(split_part + static_cast<int64_t>(q) * G.n_rows + row[i]);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (ok[i]) {
+              const float out = scale_softcap(acc[i], G.scale, G.cap);
+              G.out[row[i]] = out;
+              best = umax64(best, argmax_key(out, static_cast<uint32_t>(row[i])));
+            }
+          }
+        }
+        __syncthreads();                        // s_list and s_nlast are rewritten next round
+      }
+      for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
+      if (lane == 0 && best != 0ull) atomicMax(s_best, best);
+    }
+    __syncthreads();
+  }
   if (lse_parts && tid == 0) {                  // this CTA's pair, in a fixed order
     const MaxSum c = ms_combine({s_ms[0].x, s_ms[0].y}, {s_ms[1].x, s_ms[1].y});
     lse_parts[blockIdx.x] = make_float2(c.m, c.s);
@@ -544,26 +669,30 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
   if (argmax) argmax_publish_finish(keys, ticket, argmax, s_best, 1);
 }
 
-template <int NB, bool kGroup, bool kQ4>
+template <int NB, bool kGroup, bool kQ4, bool kSplit = false>
 cudaError_t launch_b1_nb(const float *hidden, const float *gamma, float eps, const SegTable &T,
                          unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status,
-                         float2 *lse_parts, int num_sms, cudaStream_t stream) {
+                         float2 *lse_parts, int num_sms, cudaStream_t stream, int n_chunks = 1,
+                         float *split_part = nullptr, unsigned int *split_cnt = nullptr) {
   using C = B1Cfg<NB, kQ4>;
-  static unsigned long long configured = 0;   // one bit per device: the attribute is per device
+  static std::atomic<unsigned long long> configured{0};   // one bit per device: the attribute is per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
-  if (!(configured & bit)) {
-    e = cudaFuncSetAttribute(gemv_b1_kernel<NB, kGroup, kQ4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(gemv_b1_kernel<NB, kGroup, kQ4, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured |= bit;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   const int64_t n_tiles = T.tile_end[T.n - 1];
-  const int64_t grid = n_tiles < num_sms ? n_tiles : num_sms;
-  gemv_b1_kernel<NB, kGroup, kQ4><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
-      hidden, gamma, eps, T, keys, ticket, argmax, status, lse_parts);
+  // split along K: n_chunks row tiles per tile of rows, at least one CTA per chunk
+  const int64_t units = n_tiles * n_chunks;
+  const int64_t grid = units < num_sms ? units : num_sms;
+  if (kSplit && (n_chunks < 2 || grid < n_chunks || !split_part || !split_cnt)) return cudaErrorInvalidValue;
+  gemv_b1_kernel<NB, kGroup, kQ4, kSplit><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
+      hidden, gamma, eps, T, keys, ticket, argmax, status, lse_parts, n_chunks, split_part, split_cnt);
   return cudaGetLastError();
 }
 
@@ -582,6 +711,46 @@ SegTable make_table(const GemvSegment *segs, int n) {
 }  // namespace
 
 bool b1_supported(int k) { return k == 26 * kBlockWeights || k == 16 * kBlockWeights; }
+
+// Chunk width (26 or 16 blocks) and count of a split-K batch-1 launch.
+static void split_shape(int k, int &chunk_nb, int &chunks) {
+  const int nb = k / kBlockWeights;
+  chunk_nb = nb % 26 == 0 ? 26 : nb % 16 == 0 ? 16 : 0;
+  chunks = chunk_nb ? nb / chunk_nb : 0;
+}
+
+int b1_split_chunks(int k) {
+  int cnb, s;
+  split_shape(k, cnb, s);
+  return k % kBlockWeights == 0 && s >= 2 && s <= kMaxSplitChunks ? s : 0;
+}
+
+size_t b1_split_floats(int64_t n_rows, int k) { return static_cast<size_t>(n_rows) * b1_split_chunks(k); }
+
+size_t b1_split_counters(int64_t n_rows) { return static_cast<size_t>((n_rows + kRows - 1) / kRows); }
+
+cudaError_t launch_b1_split(const LaunchArgs &a) {
+  int cnb, s;
+  split_shape(a.k, cnb, s);
+  if (b1_split_chunks(a.k) == 0 || a.num_sms < s) return cudaErrorInvalidValue;
+  const GemvSegment one = {a.w, a.logits, a.n_rows, a.scale, a.cap};
+  const SegTable T = make_table(&one, 1);
+  // no (max, sum exp) pairs: which CTA finishes a row varies from run to run,
+  // so the logprobs take the separate pass over the logits (fixed order)
+  float2 *parts = nullptr;
+  float *part = a.ws.b1_part;
+  unsigned int *cnt = a.ws.b1_cnt;
+  if (cnb == 26)
+    return a.q4 ? launch_b1_nb<26, false, true, true>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
+                                                      a.ws.status, parts, a.num_sms, a.stream, s, part, cnt)
+                : launch_b1_nb<26, false, false, true>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket,
+                                                       a.argmax, a.ws.status, parts, a.num_sms, a.stream, s, part,
+                                                       cnt);
+  return a.q4 ? launch_b1_nb<16, false, true, true>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
+                                                    a.ws.status, parts, a.num_sms, a.stream, s, part, cnt)
+              : launch_b1_nb<16, false, false, true>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
+                                                     a.ws.status, parts, a.num_sms, a.stream, s, part, cnt);
+}
 
 int b1_grid(int64_t n_rows, int num_sms) {
   const int64_t n_tiles = (n_rows + kRows - 1) / kRows;

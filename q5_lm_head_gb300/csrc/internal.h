@@ -21,6 +21,8 @@ struct Workspace {
   float2 *lse_parts;         // [MUSE_MAX_BATCH][kMaxLseParts] (max, sum exp) partials of the logprobs
   float *split_part;         // tensor-core path: [num_sms][2][128][slots] partial sums of shared tiles
   unsigned int *split_cnt;   // [num_sms][8] arrivals per shared tile and warp (per CTA boundary, or per tile when tiles < SMs), zero between forwards
+  float *b1_part;            // split-K batch-1 path: [chunks][n_rows] chunk partial sums
+  unsigned int *b1_cnt;      // split-K batch-1 path: [12-row tiles] chunk arrivals, zero between forwards
 };
 
 constexpr int kMaxLseParts = 256;
@@ -71,6 +73,15 @@ cudaError_t launch_lse_parts(const float *logits, int batch, int64_t n_rows, flo
 cudaError_t launch_logprob_apply(float *logits, int batch, int64_t n_rows, const float2 *parts, int n_parts,
                                  float *lse, cudaStream_t stream);
 int b1_grid(int64_t n_rows, int num_sms);   // CTAs of the batch-1 kernel = its (max, sum exp) pairs
+
+// Batch 1 at a K of S (2..kMaxSplitChunks) chunks of a built width (6,656 or
+// 4,096 columns): the batch-1 kernel split along K (one chunk per CTA, chunk
+// partial sums combined by the last CTA of each row tile).
+constexpr int kMaxSplitChunks = 16;
+int b1_split_chunks(int k);                          // S, or 0 when K does not split so
+size_t b1_split_floats(int64_t n_rows, int k);       // b1_part size
+size_t b1_split_counters(int64_t n_rows);            // b1_cnt size
+cudaError_t launch_b1_split(const LaunchArgs &a);
 
 // One-thread kernel whose bounded wait on a never-completed mbarrier gives up
 // and sets kStatusWaitTimeout in *status.

@@ -24,6 +24,7 @@ struct muse_lmhead {
   muse::Workspace ws;
   void *ws_base;           // single device allocation backing ws
   size_t ws_split_cnt_bytes;  // size of ws.split_cnt (0 without the tensor-core path)
+  size_t ws_b1_cnt_bytes;     // size of ws.b1_cnt (0 without the split-K batch-1 path)
   CUtensorMap wmap;        // weight tensor map of the tensor-core path, for wmap_ptr
   const void *wmap_ptr;
   float *stage_hidden;     // forward_host staging (lazy)
@@ -56,10 +57,20 @@ struct DeviceGuard {
   }
 };
 
-enum class Path { B1, TensorCore, Generic };
+enum class Path { B1, B1Split, TensorCore, Generic };
+
+// Partial sums of the split-K batch-1 path are [chunks][n_rows] floats: taken
+// only while that stays within this bound (larger handles use the tensor cores).
+constexpr size_t kMaxSplitFloats = size_t{1} << 26;
+
+bool b1_split_ok(int64_t n_rows, int64_t k) {
+  return muse::b1_split_chunks(static_cast<int>(k)) > 0 &&
+         muse::b1_split_floats(n_rows, static_cast<int>(k)) <= kMaxSplitFloats;
+}
 
 Path choose_path(const muse_lmhead *h, int batch) {
   if (batch == 1 && muse::b1_supported(static_cast<int>(h->k))) return Path::B1;
+  if (batch == 1 && b1_split_ok(h->n_rows, h->k)) return Path::B1Split;
   if (muse::tc_supported(batch, static_cast<int>(h->k))) return Path::TensorCore;
   return Path::Generic;
 }
@@ -99,6 +110,9 @@ int run_forward(muse_lmhead *h, const float *hidden, int batch, const float *gam
   cudaError_t e;
   switch (choose_path(h, batch)) {
     case Path::B1: e = muse::launch_b1(a); break;
+    case Path::B1Split:
+      e = h->ws.b1_part && h->ws.b1_cnt ? muse::launch_b1_split(a) : cudaErrorInvalidValue;
+      break;
     case Path::TensorCore:
       if (!h->ws.xpkg || !h->ws.split_cnt || !h->ws.split_part) {   // never launch without its workspace
         e = cudaErrorInvalidValue;
@@ -153,19 +167,23 @@ int muse_lmhead_init_format(muse_lmhead **out, int device, int64_t n_rows, int64
   h->num_sms = prop.multiProcessorCount;
 
   // One zeroed allocation: keys | ticket | status | logprob pairs | x | activation packages |
-  // shared-tile counters | shared-tile partial sums (the last three for the tensor-core path)
+  // shared-tile counters | shared-tile partial sums (those three for the tensor-core path) |
+  // chunk counters | chunk partial sums (the split-K batch-1 path)
   const size_t keys_b = sizeof(unsigned long long) * MUSE_MAX_BATCH;
   const size_t misc_b = 256;
   const size_t lse_b = sizeof(float2) * static_cast<size_t>(max_batch) * muse::kMaxLseParts;
   const size_t x_b = sizeof(float) * static_cast<size_t>(max_batch) * static_cast<size_t>(k);
   // the tensor-core path's workspace, wherever some batch size of this handle
   // takes that path (batch 1 does for a K without a fused batch-1 build)
+  const bool split = b1_split_ok(n_rows, k);
   const bool tc = muse::tc_supported(max_batch, static_cast<int>(k)) &&
-                  (max_batch >= 2 || !muse::b1_supported(static_cast<int>(k)));
+                  (max_batch >= 2 || (!muse::b1_supported(static_cast<int>(k)) && !split));
   const size_t pkg_b = tc ? muse::tc_workspace_bytes(static_cast<int>(k)) : 0;
   const size_t cnt_b = tc ? (sizeof(unsigned int) * muse::tc_split_counters(h->num_sms) + 255) / 256 * 256 : 0;
   const size_t part_b = tc ? sizeof(float) * muse::tc_split_floats(h->num_sms, max_batch) : 0;
-  const size_t total = keys_b + misc_b + lse_b + x_b + pkg_b + cnt_b + part_b;
+  const size_t bcnt_b = split ? (sizeof(unsigned int) * muse::b1_split_counters(n_rows) + 255) / 256 * 256 : 0;
+  const size_t bpart_b = split ? sizeof(float) * muse::b1_split_floats(n_rows, static_cast<int>(k)) : 0;
+  const size_t total = keys_b + misc_b + lse_b + x_b + pkg_b + cnt_b + part_b + bcnt_b + bpart_b;
   void *base = nullptr;
   e = cudaMalloc(&base, total);
   if (e != cudaSuccess) {
@@ -189,6 +207,11 @@ int muse_lmhead_init_format(muse_lmhead **out, int device, int64_t n_rows, int64
   h->ws.split_cnt = cnt_b ? reinterpret_cast<unsigned int *>(p + keys_b + misc_b + lse_b + x_b + pkg_b) : nullptr;
   h->ws.split_part = part_b ? reinterpret_cast<float *>(p + keys_b + misc_b + lse_b + x_b + pkg_b + cnt_b) : nullptr;
   h->ws_split_cnt_bytes = cnt_b;
+  // part_b is a multiple of 256 bytes (num_sms * 2 * 128 * slots floats)
+  uint8_t *pb = p + keys_b + misc_b + lse_b + x_b + pkg_b + cnt_b + part_b;
+  h->ws.b1_cnt = bcnt_b ? reinterpret_cast<unsigned int *>(pb) : nullptr;
+  h->ws.b1_part = bpart_b ? reinterpret_cast<float *>(pb + bcnt_b) : nullptr;
+  h->ws_b1_cnt_bytes = bcnt_b;
   *out = h;
   return MUSE_OK;
 }
@@ -227,6 +250,7 @@ int muse_lmhead_forward_logprobs(muse_lmhead *h, const float *hidden, int batch,
   if (!g.ok) return MUSE_ERR_DEVICE;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the batch-1 kernel leaves one (max, sum exp) pair per CTA; other paths get a pass over the logits
+  // (the split-K kernel too: which CTA finishes a row varies, the pass keeps the sum's order fixed)
   const bool fused = choose_path(h, batch) == Path::B1;
   st = run_forward(h, hidden, batch, gamma, eps, weights, scale, cap, logprobs, argmax, s, fused);
   if (st != MUSE_OK) return st;
@@ -335,7 +359,8 @@ int muse_lmhead_launches_per_forward(const muse_lmhead *h, int batch, int with_n
   if (!h) return MUSE_ERR_NULL;
   if (batch < 1 || batch > h->max_batch) return MUSE_ERR_BATCH;
   switch (choose_path(h, batch)) {
-    case Path::B1: return 1;
+    case Path::B1:
+    case Path::B1Split: return 1;
     case Path::TensorCore: return 2;   // activation-package prep + tcgen05 kernel
     default: return with_norm ? 2 : 1;  // generic: RMSNorm pre-pass + GEMV
   }
@@ -345,6 +370,7 @@ const char *muse_lmhead_path_name(const muse_lmhead *h, int batch) {
   if (!h || batch < 1 || batch > h->max_batch) return nullptr;
   switch (choose_path(h, batch)) {
     case Path::B1: return "gemv_b1";
+    case Path::B1Split: return "gemv_b1_split";
     case Path::TensorCore: return "gemm_tc";
     default: return "gemv_generic";
   }
@@ -363,9 +389,11 @@ int muse_lmhead_clear_device_status(muse_lmhead *h, void *stream) {
   DeviceGuard g(h->device);
   if (!g.ok) return MUSE_ERR_DEVICE;
   cudaError_t e = cudaMemsetAsync(h->ws.status, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream));
-  // a forward that gave up may have left a shared-tile counter counted in
+  // a forward that gave up may have left a shared-tile or chunk counter counted in
   if (e == cudaSuccess && h->ws.split_cnt)
     e = cudaMemsetAsync(h->ws.split_cnt, 0, h->ws_split_cnt_bytes, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess && h->ws.b1_cnt)
+    e = cudaMemsetAsync(h->ws.b1_cnt, 0, h->ws_b1_cnt_bytes, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
 }
 

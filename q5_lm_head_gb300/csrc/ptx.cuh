@@ -27,6 +27,11 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Acquire-release fence at GPU scope: orders this thread's earlier memory
+// operations, and those it has observed (for example through a CTA barrier),
+// before its later ones, for every thread of the GPU.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");

@@ -157,11 +157,11 @@ def test_q4k_grouped_call(torch_cuda, k, shapes):
         assert np.abs(out.cpu().numpy().astype(np.float64) - ref).max() <= TOL
 
 
-@pytest.mark.parametrize("name,path", [("ffn_up_q4k", "gemv_b1"), ("ffn_down_q4k", "gemm_tc")])
+@pytest.mark.parametrize("name,path", [("ffn_up_q4k", "gemv_b1"), ("ffn_down_q4k", "gemv_b1_split")])
 def test_q4k_ffn_shapes(torch_cuda, name, path):
     """One block's FFN shapes in Q4_K at batch 1: gate/up [6656 -> 19968] on the
-    fused kernel, down [19968 -> 6656] (78 blocks per row, no fused build) on the
-    tensor-core kernel with one batch row."""
+    fused kernel, down [19968 -> 6656] (78 blocks per row: three chunks of the
+    6,656-column build) on the fused kernel split along K."""
     wl = synth.WORKLOADS[name]
     hidden, gamma, wq = synth.inputs_for(wl)
     got, _ = _run(torch_cuda, hidden, gamma, wq, wl.n_rows, wl.k, wl.scale, wl.cap, path, want_argmax=False)

@@ -41,7 +41,8 @@ def _dev(torch, a):
 
 @pytest.mark.parametrize("n,k,b,path", [(2048, 6656, 1, "gemv_b1"), (3000, 6656, 4, "gemm_tc"),
                                         (20000, 6656, 8, "gemm_tc"),    # tiles shared by two CTAs
-                                        (500, 768, 2, "gemv_generic")])
+                                        (500, 768, 2, "gemv_generic"),
+                                        (1000, 13312, 1, "gemv_b1_split")])   # chunk partials via the counters
 def test_forward_replayed_from_a_cuda_graph_matches_eager(torch_cuda, n, k, b, path):
     import q5_lm_head_gb300 as mlh
     torch = torch_cuda
