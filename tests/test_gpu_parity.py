@@ -167,10 +167,10 @@ def _edge_rows(k):
                      (base * 1e15).astype(np.float32)])
 
 
-@pytest.mark.parametrize("b,path", [(1, "gemv_b1"), (4, "gemm_tc")])
-def test_edge_hidden_rows(torch_cuda, b, path):
+@pytest.mark.parametrize("b,k,path", [(1, 6656, "gemv_b1"), (4, 6656, "gemm_tc"), (1, 13312, "gemv_b1_split")])
+def test_edge_hidden_rows(torch_cuda, b, k, path):
     import q5_lm_head_gb300 as mlh
-    n, k = 3000, 6656
+    n = 3000
     rows = _edge_rows(k)
     wq = synth.q5k_matrix(n, k, synth.stream_key(11, "W:edge"), boost_rows=(7,), boost=40.0)
     gamma = synth.normal_f64(k, synth.stream_key(11, "G:edge"), 1.0, 0.1).astype(np.float32)
@@ -280,14 +280,15 @@ def test_forward_host_matches_device_forward(torch_cuda):
     assert torch.equal(ld.cpu(), lp) and torch.equal(ad.cpu(), ap) and torch.equal(ad.cpu(), ao)
 
 
-@pytest.mark.parametrize("b,path", [(4, "gemm_tc"), (1, "gemv_b1")])
-def test_forward_host_batches_and_repeats(torch_cuda, b, path):
-    """Host-buffer forwards on the batch-1 and tensor-core paths, three calls in
-    a row with changing rows: each sees its own rows and matches the device
-    forward bit for bit and the oracle within the bar."""
+@pytest.mark.parametrize("b,k,path", [(4, 6656, "gemm_tc"), (1, 6656, "gemv_b1"), (1, 13312, "gemv_b1_split")])
+def test_forward_host_batches_and_repeats(torch_cuda, b, k, path):
+    """Host-buffer forwards on the batch-1 (whole and split along K) and
+    tensor-core paths, three calls in a row with changing rows: each sees its
+    own rows and matches the device forward bit for bit and the oracle within
+    the bar."""
     import q5_lm_head_gb300 as mlh
     torch = torch_cuda
-    n, k = 5000, 6656
+    n = 5000
     wq = synth.q5k_matrix(n, k, synth.stream_key(6, "W:host"), boost_rows=(17,), boost=40.0)
     gamma = synth.normal_f64(k, synth.stream_key(6, "G:host"), 1.0, 0.1).astype(np.float32)
     rows = [synth.normal_f64(b * k, synth.stream_key(6 + i, "H:host")).astype(np.float32).reshape(b, k)

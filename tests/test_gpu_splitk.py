@@ -67,6 +67,7 @@ SHAPES = [
     (2000, 19968, "q5_k", True, 20.0),      # 3 chunks (the FFN down width)
     (777, 13312, "q4_k", True, 20.0),
     (130, 32768, "q4_k", False, 0.0),       # 8 chunks of 4,096
+    (50, 65536, "q5_k", True, 20.0),        # 16 chunks of 4,096: the most the split build takes
 ]
 
 
