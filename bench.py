@@ -236,7 +236,8 @@ def _config(wl, ws, l2_mode):
     import q5k_synth as synth
     if isinstance(wl, synth.GroupWorkload):
         return {"workload": wl.name, "matrices": [[n, r] for (n, r, _, _, _) in wl.segments], "k": wl.k,
-                "batch": 1, "weights": "Q5_K 176 B / 256 weights", "norm": wl.norm,
+                "batch": 1, "weights": "Q5_K 176 B / 256 weights" if wl.fmt == "q5_k" else "Q4_K 144 B / 256 weights",
+                "norm": wl.norm,
                 "scale_cap": [[sc, cp] for (_, _, _, sc, cp) in wl.segments], "launches": 1, "l2": l2_mode,
                 "parallelism": f"replicas x{ws}"}
     return {"workload": wl.name, "n_rows": wl.n_rows, "k": wl.k, "batch": wl.batch,
@@ -300,29 +301,21 @@ def _graph_times(fwd, stream, steps, l2_flush):
 
 
 def _e2e_group(args, wl, head, hidden, segs, g_d, eps, stream, nbytes):
-    """The grouped forward end to end: pinned hidden row copied in, every
-    matrix's output copied out to pinned host buffers, stream synchronised."""
+    """The grouped forward end to end through muse_lmhead_forward_group_host:
+    each step copies the pinned hidden row in, the kernel writes every
+    matrix's output into pinned host buffers, and the call waits for it."""
     import torch
-    h_pin = torch.from_numpy(hidden).pin_memory()
-    h_dev = torch.empty(h_pin.shape, dtype=torch.float32, device=segs[0][0].device)
-    o_pin = [torch.empty((n,), dtype=torch.float32, pin_memory=True) for (_, n, _, _, _) in segs]
+    h_pin = torch.from_numpy(hidden).reshape(-1).pin_memory()
+    host_segs = [(w, n, sc, cp, torch.empty((n,), dtype=torch.float32, pin_memory=True))
+                 for (w, n, sc, cp, _) in segs]
     steps = max(3, min(args.steps, 50))
-
-    def step():
-        with torch.cuda.stream(stream):
-            h_dev.copy_(h_pin, non_blocking=True)
-            outs = head.forward_group(h_dev, segs, g_d, eps, stream)
-            for o_h, o_d in zip(o_pin, outs):
-                o_h.copy_(o_d, non_blocking=True)
-        stream.synchronize()
-
     for _ in range(2):
-        step()
+        head.forward_group_host(h_pin, host_segs, g_d, eps, stream)
     t0 = time.perf_counter()
     for _ in range(steps):
-        step()
+        head.forward_group_host(h_pin, host_segs, g_d, eps, stream)
     secs = (time.perf_counter() - t0) / steps
-    value, secs = replica_aggregate(secs, nbytes, h_dev.device)
+    value, secs = replica_aggregate(secs, nbytes, g_d.device if g_d is not None else segs[0][0].device)
     return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": wl.k * 4,
             "d2h_bytes_per_step": wl.n_rows * 4, "us_per_forward": round(secs * 1e6, 2)}
 
@@ -367,7 +360,7 @@ def _oracle_rate_group(g, hidden, gamma, wqs, target_s: float):
     t0 = time.perf_counter()
     while True:
         for w, (_, n, _, sc, cp) in zip(wqs, g.segments):
-            oracle.lmhead(hidden, gamma, w, sc, cp, nthreads=cores)
+            oracle.lmhead(hidden, gamma, w, sc, cp, nthreads=cores, fmt=g.fmt)
         reps += 1
         secs = time.perf_counter() - t0
         if secs >= target_s:
@@ -400,7 +393,7 @@ def run_ours(args, wl):
     if group:
         hidden, gamma, wq = synth.group_inputs(wl)     # wq: one weight matrix per segment
         w_d = [torch.from_numpy(w).to(dev) for w in wq]
-        head = mlh.LMHead(1, wl.k, max_batch=1, device=local)
+        head = mlh.LMHead(1, wl.k, max_batch=1, device=local, fmt=wl.fmt)
         outs = [torch.empty((n,), dtype=torch.float32, device=dev) for (_, n, _, _, _) in wl.segments]
         segs = [(w, n, sc, cp, o) for w, o, (_, n, _, sc, cp) in zip(w_d, outs, wl.segments)]
         path, launches = "gemv_b1_group", 1

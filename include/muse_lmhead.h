@@ -263,6 +263,22 @@ int muse_lmhead_forward_group(muse_lmhead *h, const float *hidden, const float *
                               float eps, const muse_gemv_segment *segments,
                               int n_segments, void *stream);
 
+/*
+ * The grouped forward for callers whose input row and outputs live in host
+ * memory: copies hidden_host ([k] f32, host, any alignment) to the device,
+ * runs muse_lmhead_forward_group, brings every segment's output back, and
+ * waits for `stream` before returning.  gamma and each segment's weights are
+ * device pointers; each segments[s].out is a HOST buffer of n_rows floats
+ * (4-byte aligned).  An output that is page-locked for this device is written
+ * by the kernel directly through the device's mapping of host memory; a
+ * pageable one goes through a device staging buffer that the handle keeps
+ * (grown on demand; growing it waits for `stream` first).  Validation as for
+ * muse_lmhead_forward_group.
+ */
+int muse_lmhead_forward_group_host(muse_lmhead *h, const float *hidden_host, const float *gamma,
+                                   float eps, const muse_gemv_segment *segments,
+                                   int n_segments, void *stream);
+
 /* Free the handle and its workspace.  NULL is allowed.  Must not be called
  * while a forward using the handle may still be running on the GPU. */
 void muse_lmhead_destroy(muse_lmhead *h);

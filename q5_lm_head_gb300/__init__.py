@@ -19,7 +19,8 @@ __all__ = [
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
-    "muse_lmhead_forward_group", "MuseGemvSegment", "MUSE_MAX_SEGMENTS", "muse_lmhead_forward_logprobs",
+    "muse_lmhead_forward_group", "muse_lmhead_forward_group_host", "MuseGemvSegment", "MUSE_MAX_SEGMENTS",
+    "muse_lmhead_forward_logprobs",
     "muse_lmhead_init_format", "MUSE_FORMAT_Q5_K", "MUSE_FORMAT_Q4_K", "BLOCK_BYTES",
     "muse_lmhead_clear_device_status", "muse_lmhead_selftest_wait_timeout",
     "EXPORTED_SYMBOLS",
@@ -40,7 +41,8 @@ EXPORTED_SYMBOLS = (
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
-    "muse_lmhead_forward_group", "muse_lmhead_forward_logprobs", "muse_lmhead_init_format",
+    "muse_lmhead_forward_group", "muse_lmhead_forward_group_host", "muse_lmhead_forward_logprobs",
+    "muse_lmhead_init_format",
     "muse_lmhead_clear_device_status", "muse_lmhead_selftest_wait_timeout",
 )
 
@@ -111,6 +113,8 @@ def load_library():
     lib.muse_lmhead_forward_logprobs.argtypes = [vp, vp, i32, vp, f32, vp, f32, f32, vp, vp, vp, vp]
     lib.muse_lmhead_forward_group.restype = i32
     lib.muse_lmhead_forward_group.argtypes = [vp, vp, vp, f32, ctypes.POINTER(MuseGemvSegment), i32, vp]
+    lib.muse_lmhead_forward_group_host.restype = i32
+    lib.muse_lmhead_forward_group_host.argtypes = [vp, vp, vp, f32, ctypes.POINTER(MuseGemvSegment), i32, vp]
     _lib = lib
     return lib
 
@@ -204,6 +208,15 @@ def muse_lmhead_forward_group(h: int | None, hidden: int, gamma: int | None, eps
     for i, (w, n, o, sc, cp) in enumerate(segments):
         arr[i] = MuseGemvSegment(w, n, o, sc, cp)
     return load_library().muse_lmhead_forward_group(h, hidden, gamma, eps, arr, len(segments), stream)
+
+
+def muse_lmhead_forward_group_host(h: int | None, hidden_host: int, gamma: int | None, eps: float, segments,
+                                   stream: int | None) -> int:
+    """segments: sequence of (weights_ptr (device), n_rows, out_ptr (host), scale, cap)."""
+    arr = (MuseGemvSegment * max(1, len(segments)))()
+    for i, (w, n, o, sc, cp) in enumerate(segments):
+        arr[i] = MuseGemvSegment(w, n, o, sc, cp)
+    return load_library().muse_lmhead_forward_group_host(h, hidden_host, gamma, eps, arr, len(segments), stream)
 
 
 class LMHead:
@@ -350,6 +363,33 @@ class LMHead:
         st = muse_lmhead_forward_group(self.handle, hp, gp, float(eps), descs, s.cuda_stream)
         if st != MUSE_OK:
             raise MuseError(st, "muse_lmhead_forward_group")
+        return outs
+
+    def forward_group_host(self, hidden_host, segments, gamma=None, eps: float = RMS_EPS, stream=None):
+        """The grouped forward from host memory: hidden_host [k] (or [1, k]) f32
+        CPU tensor; segments: sequence of (weights uint8 tensor on the GPU,
+        n_rows, scale, cap, out CPU tensor or None).  Outputs default to pinned
+        CPU tensors, which the kernel writes directly; returns them."""
+        import torch
+        h = hidden_host.reshape(-1)
+        if h.device.type != "cpu" or h.dtype != torch.float32 or not h.is_contiguous() or h.numel() != self.k:
+            raise ValueError("hidden_host: need a contiguous f32 CPU tensor of k values")
+        gp = None if gamma is None else self._check(gamma, "gamma", torch.float32, (self.k,))
+        outs, descs = [], []
+        for (w, n, scale, cap, out) in segments:
+            wp = self._check(w, "weights", torch.uint8)
+            if w.numel() != n * (self.k // 256) * self.block_bytes:
+                raise ValueError("weights: wrong number of bytes for n_rows")
+            if out is None:
+                out = torch.empty((n,), dtype=torch.float32, pin_memory=True)
+            if out.device.type != "cpu" or out.dtype != torch.float32 or not out.is_contiguous() or out.numel() != n:
+                raise ValueError("out: need a contiguous f32 CPU tensor of n_rows values")
+            outs.append(out)
+            descs.append((wp, n, out.data_ptr(), float(scale), float(cap)))
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        st = muse_lmhead_forward_group_host(self.handle, h.data_ptr(), gp, float(eps), descs, s.cuda_stream)
+        if st != MUSE_OK:
+            raise MuseError(st, "muse_lmhead_forward_group_host")
         return outs
 
     def path_name(self, batch: int) -> str | None:

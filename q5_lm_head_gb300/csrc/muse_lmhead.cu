@@ -30,6 +30,8 @@ struct muse_lmhead {
   float *stage_hidden;     // forward_host staging (lazy)
   float *stage_logits;
   int32_t *stage_argmax;
+  float *stage_group;      // forward_group_host staging of pageable outputs (lazy, grows)
+  int64_t stage_group_n;   // its size in floats
 };
 
 namespace {
@@ -216,14 +218,17 @@ int muse_lmhead_init_format(muse_lmhead **out, int device, int64_t n_rows, int64
   return MUSE_OK;
 }
 
-int muse_lmhead_forward_group(muse_lmhead *h, const float *hidden, const float *gamma, float eps,
-                              const muse_gemv_segment *segments, int n_segments, void *stream) {
+namespace {
+
+// Checks shared by the grouped calls (hidden may be a host or device pointer:
+// the caller checks what it needs of it); fills segs.
+int validate_group(const muse_lmhead *h, const float *hidden, const float *gamma, float eps,
+                   const muse_gemv_segment *segments, int n_segments, muse::GemvSegment *segs) {
   if (!h || !hidden || !segments) return MUSE_ERR_NULL;
   if (n_segments < 1 || n_segments > MUSE_MAX_SEGMENTS) return MUSE_ERR_SHAPE;
   if (!muse::b1_supported(static_cast<int>(h->k))) return MUSE_ERR_SHAPE;
   if (gamma && (!std::isfinite(eps) || eps < 0.0f)) return MUSE_ERR_VALUE;
-  if (!aligned(hidden, 16) || (gamma && !aligned(gamma, 16))) return MUSE_ERR_ALIGN;
-  muse::GemvSegment segs[muse::kMaxSegments];
+  if (gamma && !aligned(gamma, 16)) return MUSE_ERR_ALIGN;
   for (int i = 0; i < n_segments; ++i) {
     const muse_gemv_segment &g = segments[i];
     if (!g.weights || !g.out) return MUSE_ERR_NULL;
@@ -232,12 +237,47 @@ int muse_lmhead_forward_group(muse_lmhead *h, const float *hidden, const float *
     if (!aligned(g.weights, 16) || !aligned(g.out, 4)) return MUSE_ERR_ALIGN;
     segs[i] = {static_cast<const uint8_t *>(g.weights), g.out, g.n_rows, g.scale, g.cap};
   }
+  return MUSE_OK;
+}
+
+int run_group(muse_lmhead *h, const float *hidden, const float *gamma, float eps, const muse::GemvSegment *segs,
+              int n_segments, cudaStream_t stream) {
+  const cudaError_t e = muse::launch_b1_group(hidden, gamma, eps, static_cast<int>(h->k), segs, n_segments,
+                                              h->ws.status, h->num_sms, stream, h->format == MUSE_FORMAT_Q4_K);
+  return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
+}
+
+// The forward_host staging buffers (max_batch rows of input and logits, the argmax), allocated once.
+int ensure_host_staging(muse_lmhead *h) {
+  if (h->stage_hidden) return MUSE_OK;
+  const size_t hb = sizeof(float) * h->max_batch * h->k;
+  const size_t lb = sizeof(float) * h->max_batch * h->n_rows;
+  const size_t ab = sizeof(int32_t) * MUSE_MAX_BATCH;
+  void *p1 = nullptr, *p2 = nullptr, *p3 = nullptr;
+  cudaError_t e;
+  if ((e = cudaMalloc(&p1, hb)) != cudaSuccess || (e = cudaMalloc(&p2, lb)) != cudaSuccess ||
+      (e = cudaMalloc(&p3, ab)) != cudaSuccess) {
+    if (p1) cudaFree(p1);
+    if (p2) cudaFree(p2);
+    return e == cudaErrorMemoryAllocation ? MUSE_ERR_NOMEM : cuda_fail(e);
+  }
+  h->stage_hidden = static_cast<float *>(p1);
+  h->stage_logits = static_cast<float *>(p2);
+  h->stage_argmax = static_cast<int32_t *>(p3);
+  return MUSE_OK;
+}
+
+}  // namespace
+
+int muse_lmhead_forward_group(muse_lmhead *h, const float *hidden, const float *gamma, float eps,
+                              const muse_gemv_segment *segments, int n_segments, void *stream) {
+  muse::GemvSegment segs[muse::kMaxSegments];
+  const int st = validate_group(h, hidden, gamma, eps, segments, n_segments, segs);
+  if (st != MUSE_OK) return st;
+  if (!aligned(hidden, 16)) return MUSE_ERR_ALIGN;
   DeviceGuard dg(h->device);
   if (!dg.ok) return MUSE_ERR_DEVICE;
-  const cudaError_t e = muse::launch_b1_group(hidden, gamma, eps, static_cast<int>(h->k), segs, n_segments,
-                                              h->ws.status, h->num_sms, static_cast<cudaStream_t>(stream),
-                                              h->format == MUSE_FORMAT_Q4_K);
-  return e == cudaSuccess ? MUSE_OK : cuda_fail(e);
+  return run_group(h, hidden, gamma, eps, segs, n_segments, static_cast<cudaStream_t>(stream));
 }
 
 int muse_lmhead_forward_logprobs(muse_lmhead *h, const float *hidden, int batch, const float *gamma, float eps,
@@ -307,21 +347,7 @@ int muse_lmhead_forward_host(muse_lmhead *h, const float *hidden_host, int batch
   DeviceGuard g(h->device);
   if (!g.ok) return MUSE_ERR_DEVICE;
   cudaError_t e;
-  if (!h->stage_hidden) {
-    const size_t hb = sizeof(float) * h->max_batch * h->k;
-    const size_t lb = sizeof(float) * h->max_batch * h->n_rows;
-    const size_t ab = sizeof(int32_t) * MUSE_MAX_BATCH;
-    void *p1 = nullptr, *p2 = nullptr, *p3 = nullptr;
-    if ((e = cudaMalloc(&p1, hb)) != cudaSuccess || (e = cudaMalloc(&p2, lb)) != cudaSuccess ||
-        (e = cudaMalloc(&p3, ab)) != cudaSuccess) {
-      if (p1) cudaFree(p1);
-      if (p2) cudaFree(p2);
-      return e == cudaErrorMemoryAllocation ? MUSE_ERR_NOMEM : cuda_fail(e);
-    }
-    h->stage_hidden = static_cast<float *>(p1);
-    h->stage_logits = static_cast<float *>(p2);
-    h->stage_argmax = static_cast<int32_t *>(p3);
-  }
+  if ((st = ensure_host_staging(h)) != MUSE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t in_b = sizeof(float) * static_cast<size_t>(batch) * h->k;
   if ((e = cudaMemcpyAsync(h->stage_hidden, hidden_host, in_b, cudaMemcpyHostToDevice, s)) != cudaSuccess)
@@ -348,6 +374,62 @@ int muse_lmhead_forward_host(muse_lmhead *h, const float *hidden_host, int batch
   }
   if (argmax_host) {
     if ((e = cudaMemcpyAsync(argmax_host, h->stage_argmax, sizeof(int32_t) * batch, cudaMemcpyDeviceToHost,
+                             s)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+  return MUSE_OK;
+}
+
+int muse_lmhead_forward_group_host(muse_lmhead *h, const float *hidden_host, const float *gamma, float eps,
+                                   const muse_gemv_segment *segments, int n_segments, void *stream) {
+  muse::GemvSegment segs[muse::kMaxSegments];
+  int st = validate_group(h, hidden_host, gamma, eps, segments, n_segments, segs);
+  if (st != MUSE_OK) return st;
+  DeviceGuard g(h->device);
+  if (!g.ok) return MUSE_ERR_DEVICE;
+  if ((st = ensure_host_staging(h)) != MUSE_OK) return st;
+  // page-locked outputs are written through the device's mapping of host
+  // memory; pageable ones go through the group staging buffer
+  float *host_out[muse::kMaxSegments] = {};
+  int64_t staged = 0;
+  for (int i = 0; i < n_segments; ++i) {
+    if (void *a = mapped_alias(segs[i].out, h->device)) {
+      segs[i].out = static_cast<float *>(a);
+    } else {
+      host_out[i] = segs[i].out;
+      staged += segs[i].n_rows;
+    }
+  }
+  cudaError_t e;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (staged > h->stage_group_n) {
+    if (h->stage_group) {
+      if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);   // earlier calls' copies done
+      cudaFree(h->stage_group);
+      h->stage_group = nullptr;
+      h->stage_group_n = 0;
+    }
+    void *p = nullptr;
+    if ((e = cudaMalloc(&p, sizeof(float) * static_cast<size_t>(staged))) != cudaSuccess)
+      return e == cudaErrorMemoryAllocation ? MUSE_ERR_NOMEM : cuda_fail(e);
+    h->stage_group = static_cast<float *>(p);
+    h->stage_group_n = staged;
+  }
+  int64_t off = 0;
+  for (int i = 0; i < n_segments; ++i) {
+    if (host_out[i]) {
+      segs[i].out = h->stage_group + off;
+      off += segs[i].n_rows;
+    }
+  }
+  if ((e = cudaMemcpyAsync(h->stage_hidden, hidden_host, sizeof(float) * h->k, cudaMemcpyHostToDevice, s)) !=
+      cudaSuccess)
+    return cuda_fail(e);
+  if ((st = run_group(h, h->stage_hidden, gamma, eps, segs, n_segments, s)) != MUSE_OK) return st;
+  for (int i = 0; i < n_segments; ++i) {
+    if (host_out[i] &&
+        (e = cudaMemcpyAsync(host_out[i], segs[i].out, sizeof(float) * segs[i].n_rows, cudaMemcpyDeviceToHost,
                              s)) != cudaSuccess)
       return cuda_fail(e);
   }
@@ -412,6 +494,7 @@ void muse_lmhead_destroy(muse_lmhead *h) {
   if (h->stage_hidden) cudaFree(h->stage_hidden);
   if (h->stage_logits) cudaFree(h->stage_logits);
   if (h->stage_argmax) cudaFree(h->stage_argmax);
+  if (h->stage_group) cudaFree(h->stage_group);
   delete h;
 }
 

@@ -266,8 +266,8 @@ WORKLOADS["lmhead_q4k_b8"] = Workload("lmhead_q4k_b8", VOCAB, HIDDEN, 8, "W:lmhe
 
 @dataclass(frozen=True)
 class GroupWorkload:
-    """Several Q5_K matrices against one input row in one launch.  segments:
-    ((name, n_rows, weight_tag, scale, cap), ...)."""
+    """Several matrices (all Q5_K or all Q4_K) against one input row in one
+    launch.  segments: ((name, n_rows, weight_tag, scale, cap), ...)."""
     name: str
     k: int
     segments: tuple
@@ -276,6 +276,7 @@ class GroupWorkload:
     gamma_tag: str = ""
     batch: int = 1
     argmax: bool = False
+    fmt: str = "q5_k"
 
     @property
     def n_rows(self) -> int:
@@ -283,10 +284,10 @@ class GroupWorkload:
 
     @property
     def weight_bytes(self) -> int:
-        return self.n_rows * (self.k // BLOCK_WEIGHTS) * BLOCK_BYTES
+        return self.n_rows * (self.k // BLOCK_WEIGHTS) * (BLOCK_BYTES if self.fmt == "q5_k" else BLOCK_BYTES_Q4K)
 
     def algorithmic_bytes(self) -> int:
-        """Q5_K weights of every matrix + hidden + gamma + outputs."""
+        """Weights of every matrix + hidden + gamma + outputs."""
         b = self.weight_bytes + self.k * 4 + self.n_rows * 4
         if self.norm:
             b += self.k * 4
@@ -300,6 +301,12 @@ GROUPS: dict[str, GroupWorkload] = {
                                (("q", 4096, "W:attn_q", 1.0, 0.0), ("gate", 4096, "W:attn_gate", 1.0, 0.0),
                                 ("k", 256, "W:attn_k", 1.0, 0.0), ("v", 256, "W:attn_v", 1.0, 0.0)),
                                hidden_tag="H:attn_qkvg", gamma_tag="G:attn_norm"),
+    # The FFN's gate and up projections [6656 -> 19968] in Q4_K from the
+    # ffn_norm-normalised residual: one launch for both (149.5 MB).
+    "ffn_gate_up_q4k": GroupWorkload("ffn_gate_up_q4k", HIDDEN,
+                                     (("gate", FFN_WIDTH, "W:ffn_gate_q4k", 1.0, 0.0),
+                                      ("up", FFN_WIDTH, "W:ffn_up_q4k", 1.0, 0.0)),
+                                     hidden_tag="H:ffn_gate_up", gamma_tag="G:ffn_norm", fmt="q4_k"),
 }
 
 
@@ -309,7 +316,7 @@ def group_inputs(g: GroupWorkload | str, seed: int = 0):
         g = GROUPS[g]
     h = normal_f64(g.k, stream_key(seed, g.hidden_tag)).reshape(1, g.k).astype(np.float32)
     gam = normal_f64(g.k, stream_key(seed, g.gamma_tag), 1.0, 0.1).astype(np.float32) if g.norm else None
-    ws = [q5k_matrix(n, g.k, stream_key(seed, tag)) for (_, n, tag, _, _) in g.segments]
+    ws = [q5k_matrix(n, g.k, stream_key(seed, tag), fmt=g.fmt) for (_, n, tag, _, _) in g.segments]
     return h, gam, ws
 
 

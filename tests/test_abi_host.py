@@ -72,6 +72,7 @@ def test_validation_fails_closed_without_cuda(lib):
     import q5_lm_head_gb300 as mlh
     seg = (mlh.MuseGemvSegment * 1)()
     assert lib.muse_lmhead_forward_group(None, 16, None, 1e-5, seg, 1, None) == -1
+    assert lib.muse_lmhead_forward_group_host(None, 16, None, 1e-5, seg, 1, None) == -1
     assert lib.muse_lmhead_forward_logprobs(None, 16, 1, None, 1e-5, 16, 1.0, 0.0, 16, None, None, None) == -1
     assert lib.muse_lmhead_clear_device_status(None, None) == -1
     assert lib.muse_lmhead_selftest_wait_timeout(None, None) == -1

@@ -32,10 +32,10 @@ def _dev(torch, a):
     return torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
 
 
-def _run_group(torch, k, hidden, gamma, mats, eps=synth.RMS_EPS):
+def _run_group(torch, k, hidden, gamma, mats, eps=synth.RMS_EPS, fmt="q5_k"):
     """mats: list of (weights_host, n_rows, scale, cap).  Returns host outputs."""
     import q5_lm_head_gb300 as mlh
-    with mlh.LMHead(1, k, max_batch=1, device=0) as head:
+    with mlh.LMHead(1, k, max_batch=1, device=0, fmt=fmt) as head:
         segs = [(_dev(torch, w), n, sc, cp, None) for (w, n, sc, cp) in mats]
         outs = head.forward_group(_dev(torch, hidden), segs, None if gamma is None else _dev(torch, gamma), eps)
         torch.cuda.synchronize()
@@ -58,6 +58,52 @@ def test_attention_qkvg_group(torch_cuda):
         ref = oracle.lmhead(hidden, gamma, w, sc, cp, synth.RMS_EPS)[0]
         assert got.shape == (n,)
         _check(got, ref, name)
+
+
+def test_ffn_gate_up_q4k_group(torch_cuda):
+    """The FFN's gate and up projections (two 19,968 x 6,656 Q4_K matrices on
+    the ffn_norm-normalised row) in one launch."""
+    g = synth.GROUPS["ffn_gate_up_q4k"]
+    hidden, gamma, ws = synth.group_inputs(g)
+    mats = [(w, n, sc, cp) for w, (_, n, _, sc, cp) in zip(ws, g.segments)]
+    outs = _run_group(torch_cuda, g.k, hidden, gamma, mats, fmt=g.fmt)
+    for (name, n, _, sc, cp), w, got in zip(g.segments, ws, outs):
+        ref = oracle.lmhead(hidden, gamma, w, sc, cp, synth.RMS_EPS, fmt=g.fmt)[0]
+        assert got.shape == (n,)
+        _check(got, ref, name)
+
+
+def test_group_from_host_buffers_matches_the_device_call(torch_cuda):
+    """muse_lmhead_forward_group_host: pinned outputs (written by the kernel
+    through the host mapping), pageable outputs (staged, copied back; the
+    staging buffer grows on the second call), the same bits as the device call."""
+    import q5_lm_head_gb300 as mlh
+    torch = torch_cuda
+    k = 6656
+    rows = (300, 5000, 12)
+    hidden = synth.normal_f64(k, synth.stream_key(13, "H:grouphost")).astype(np.float32).reshape(1, k)
+    gamma = synth.normal_f64(k, synth.stream_key(13, "G:grouphost"), 1.0, 0.1).astype(np.float32)
+    ws = [_dev(torch, synth.q5k_matrix(n, k, synth.stream_key(13, f"W:grouphost{n}"))) for n in rows]
+    caps = ((1.0, 0.0), (synth.LOGIT_SCALE, synth.SOFTCAP), (0.5, 2.0))
+    with mlh.LMHead(1, k, max_batch=1, device=0) as head:
+        g_d = _dev(torch, gamma)
+        dev = head.forward_group(_dev(torch, hidden), [(w, n, sc, cp, None) for w, n, (sc, cp) in zip(ws, rows, caps)],
+                                 g_d)
+        h_pin = torch.from_numpy(hidden).pin_memory()
+        pinned = head.forward_group_host(h_pin, [(w, n, sc, cp, None) for w, n, (sc, cp) in zip(ws, rows, caps)],
+                                         g_d)
+        small = head.forward_group_host(torch.from_numpy(hidden.copy()),       # pageable, one segment
+                                        [(ws[0], rows[0], 1.0, 0.0, torch.zeros(rows[0]))], g_d)
+        mixed = [torch.zeros(rows[0]), torch.zeros(rows[1]).pin_memory(), torch.zeros(rows[2])]
+        head.forward_group_host(h_pin, [(w, n, sc, cp, o) for w, n, (sc, cp), o in zip(ws, rows, caps, mixed)], g_d)
+        torch.cuda.synchronize()
+        assert head.device_status() == 0
+    for d, p, m in zip(dev, pinned, mixed):
+        assert torch.equal(d.cpu(), p) and torch.equal(d.cpu(), m)
+    assert torch.equal(dev[0].cpu(), small[0])
+    for i, (n, (sc, cp)) in enumerate(zip(rows, caps)):
+        ref = oracle.lmhead(hidden, gamma, ws[i].cpu().numpy(), sc, cp, synth.RMS_EPS)[0]
+        _check(pinned[i].numpy(), ref, f"segment {i}")
 
 
 @pytest.mark.parametrize("k,rows,caps,norm", [
