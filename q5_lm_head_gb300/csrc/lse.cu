@@ -7,6 +7,8 @@
 //   lse_parts_kernel     one CTA per (chunk, row): the chunk's online (max, sum exp)
 //                        pair.  The batch-1 kernel writes one such pair per CTA
 //                        from its row epilogue instead, so it needs no extra pass.
+//                        Launched as a programmatic dependent of the kernel that
+//                        wrote the logits, like the apply kernel below.
 //   logprob_apply_kernel every CTA combines the row's pairs in a fixed order
 //                        (all CTAs get the same lse bit for bit), CTA 0 stores
 //                        lse, and each CTA subtracts it from its chunk in place.
@@ -36,6 +38,7 @@ __device__ __forceinline__ MaxSum block_combine(MaxSum a, MaxSum *s_part) {
 __global__ void __launch_bounds__(kLseThreads)
     lse_parts_kernel(const float *__restrict__ logits, int64_t n_rows, int64_t chunk, float2 *__restrict__ parts) {
   __shared__ MaxSum s_part[kLseThreads / 32];
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the logits are complete
   const int b = blockIdx.y;
   const int64_t lo = static_cast<int64_t>(blockIdx.x) * chunk;
   const int64_t hi = lo + chunk < n_rows ? lo + chunk : n_rows;
@@ -82,8 +85,16 @@ int lse_parts_for(int64_t n_rows) {
 cudaError_t launch_lse_parts(const float *logits, int batch, int64_t n_rows, float2 *parts, cudaStream_t stream) {
   const int n = lse_parts_for(n_rows);
   const int64_t chunk = (n_rows + n - 1) / n;           // n chunks cover every row
-  lse_parts_kernel<<<dim3(n, batch), kLseThreads, 0, stream>>>(logits, n_rows, chunk, parts);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(n), batch);
+  cfg.blockDim = dim3(kLseThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lse_parts_kernel, logits, n_rows, chunk, parts);
 }
 
 cudaError_t launch_logprob_apply(float *logits, int batch, int64_t n_rows, const float2 *parts, int n_parts,
