@@ -279,6 +279,26 @@ int muse_lmhead_forward_group_host(muse_lmhead *h, const float *hidden_host, con
                                    float eps, const muse_gemv_segment *segments,
                                    int n_segments, void *stream);
 
+/* Argmax keys (muse_lmhead_set_argmax_key). */
+#define MUSE_ARGMAX_CAPPED 0   /* the returned logit, after scale and cap (the default) */
+#define MUSE_ARGMAX_PRECAP 1   /* scale * raw, before the cap */
+
+/*
+ * Choose what the handle's argmax ranks, for every later forward (logits and
+ * logprobs alike; the logits themselves do not change).  The cap is strictly
+ * increasing, so in exact arithmetic both keys pick the same index ("Chapter
+ * 20 — Final norm, LM head, and the soft cap", §20.2: greedy selection is
+ * invariant to the cap).  In f32 the cap merges distinct large values into
+ * ties: pre-cap values from about 170 up land on a few floats just below 20
+ * (170 and 190 both give 19.999998f; from about 200 on every value gives
+ * 20.0f), and the capped key then returns the lowest index among them, where
+ * the pre-cap key keeps their order.  Ties of the key itself go to the lowest
+ * index either way.  Host-only
+ * setting, takes effect for forwards enqueued after it; MUSE_ERR_VALUE for an
+ * unknown key.
+ */
+int muse_lmhead_set_argmax_key(muse_lmhead *h, int key);
+
 /* Free the handle and its workspace.  NULL is allowed.  Must not be called
  * while a forward using the handle may still be running on the GPU. */
 void muse_lmhead_destroy(muse_lmhead *h);

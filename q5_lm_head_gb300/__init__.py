@@ -23,6 +23,7 @@ __all__ = [
     "muse_lmhead_forward_logprobs",
     "muse_lmhead_init_format", "MUSE_FORMAT_Q5_K", "MUSE_FORMAT_Q4_K", "BLOCK_BYTES",
     "muse_lmhead_clear_device_status", "muse_lmhead_selftest_wait_timeout",
+    "muse_lmhead_set_argmax_key", "MUSE_ARGMAX_CAPPED", "MUSE_ARGMAX_PRECAP",
     "EXPORTED_SYMBOLS",
     "LOGIT_SCALE", "SOFTCAP", "RMS_EPS",
 ]
@@ -43,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
     "muse_lmhead_forward_group", "muse_lmhead_forward_group_host", "muse_lmhead_forward_logprobs",
     "muse_lmhead_init_format",
-    "muse_lmhead_clear_device_status", "muse_lmhead_selftest_wait_timeout",
+    "muse_lmhead_clear_device_status", "muse_lmhead_selftest_wait_timeout", "muse_lmhead_set_argmax_key",
 )
 
 MUSE_OK = 0
@@ -54,6 +55,9 @@ MUSE_FORMAT_Q4_K = 1
 FORMATS = {"q5_k": MUSE_FORMAT_Q5_K, "q4_k": MUSE_FORMAT_Q4_K}
 BLOCK_BYTES = {"q5_k": 176, "q4_k": 144}
 STATUS_WAIT_TIMEOUT = 1
+MUSE_ARGMAX_CAPPED = 0      # argmax key: the returned (capped) logit
+MUSE_ARGMAX_PRECAP = 1      # argmax key: scale * raw, before the cap
+ARGMAX_KEYS = {"capped": MUSE_ARGMAX_CAPPED, "precap": MUSE_ARGMAX_PRECAP}
 
 _lib = None
 
@@ -109,6 +113,8 @@ def load_library():
     lib.muse_lmhead_clear_device_status.argtypes = [vp, vp]
     lib.muse_lmhead_selftest_wait_timeout.restype = i32
     lib.muse_lmhead_selftest_wait_timeout.argtypes = [vp, vp]
+    lib.muse_lmhead_set_argmax_key.restype = i32
+    lib.muse_lmhead_set_argmax_key.argtypes = [vp, i32]
     lib.muse_lmhead_forward_logprobs.restype = i32
     lib.muse_lmhead_forward_logprobs.argtypes = [vp, vp, i32, vp, f32, vp, f32, f32, vp, vp, vp, vp]
     lib.muse_lmhead_forward_group.restype = i32
@@ -188,6 +194,10 @@ def muse_lmhead_status_string(status: int) -> str:
 # ------------------------------------------------------------ torch-facing wrapper
 def muse_lmhead_clear_device_status(h: int, stream: int | None = None) -> int:
     return load_library().muse_lmhead_clear_device_status(h, stream)
+
+
+def muse_lmhead_set_argmax_key(h: int | None, key: int) -> int:
+    return load_library().muse_lmhead_set_argmax_key(h, key)
 
 
 def muse_lmhead_selftest_wait_timeout(h: int, stream: int | None = None) -> int:
@@ -391,6 +401,14 @@ class LMHead:
         if st != MUSE_OK:
             raise MuseError(st, "muse_lmhead_forward_group_host")
         return outs
+
+    def set_argmax_key(self, key: str) -> None:
+        """"capped" (the returned logit; the default) or "precap" (scale * raw, before the cap)."""
+        if key not in ARGMAX_KEYS:
+            raise ValueError(f"argmax key: one of {sorted(ARGMAX_KEYS)}")
+        st = muse_lmhead_set_argmax_key(self.handle, ARGMAX_KEYS[key])
+        if st != MUSE_OK:
+            raise MuseError(st, "muse_lmhead_set_argmax_key")
 
     def path_name(self, batch: int) -> str | None:
         return muse_lmhead_path_name(self.handle, batch)

@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const uint8_t *__restrict__ pkgs, int nb,
                    int64_t n_rows, int batch, float scale, float cap, float *__restrict__ logits,
                    unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status,
-                   float *split_part, unsigned int *split_cnt) {
+                   float *split_part, unsigned int *split_cnt, int argmax_precap) {
   using C = TcCfg<NM, kQ4>;
   constexpr int HB = NM / 2;                                      // batch columns per warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -590,7 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float v_out = scale_softcap(v[b], scale, cap);
               const bool valid = row < n_rows;
               if (valid) logits[static_cast<size_t>(b0 + b) * n_rows + row] = v_out;
-              const unsigned long long key = warp_argmax_key(v_out, static_cast<uint32_t>(row), valid);
+              const unsigned long long key =
+                  warp_argmax_key(argmax_precap ? v[b] * scale : v_out, static_cast<uint32_t>(row), valid);
               if (lane == 0 && key != 0ull) atomicMax(&s_keys[b0 + b], key);
             }
           }
@@ -726,7 +727,7 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NM, kQ4, kNarrow>, map, static_cast<const uint8_t *>(a.ws.xpkg), nb,
                             a.n_rows, a.batch, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax,
-                            a.ws.status, a.ws.split_part, a.ws.split_cnt);
+                            a.ws.status, a.ws.split_part, a.ws.split_cnt, a.argmax_precap ? 1 : 0);
 }
 
 }  // namespace

@@ -218,6 +218,7 @@ struct SegTable {
   GemvSegment seg[kMaxSegments];
   int64_t tile_end[kMaxSegments];
   int n;
+  int argmax_precap;   // argmax key: raw * scale (before the cap) instead of the returned logit
 };
 
 // Where global tile `tile` lives: its matrix, its first row there and its rows.
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
         const float out = scale_softcap(sacc, G.scale, G.cap);
         G.out[row] = out;
         if constexpr (!kGroup) {
-          best = umax64(best, argmax_key(out, static_cast<uint32_t>(row)));
+          best = umax64(best, argmax_key(segs.argmax_precap ? sacc * G.scale : out, static_cast<uint32_t>(row)));
           if (lse_parts) ms = ms_add(ms, out);
         }
       }
@@ -651,7 +652,8 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
             if (ok[i]) {
               const float out = scale_softcap(acc[i], G.scale, G.cap);
               G.out[row[i]] = out;
-              best = umax64(best, argmax_key(out, static_cast<uint32_t>(row[i])));
+              best = umax64(best, argmax_key(segs.argmax_precap ? acc[i] * G.scale : out,
+                                             static_cast<uint32_t>(row[i])));
             }
           }
         }
@@ -734,7 +736,8 @@ cudaError_t launch_b1_split(const LaunchArgs &a) {
   split_shape(a.k, cnb, s);
   if (b1_split_chunks(a.k) == 0 || a.num_sms < s) return cudaErrorInvalidValue;
   const GemvSegment one = {a.w, a.logits, a.n_rows, a.scale, a.cap};
-  const SegTable T = make_table(&one, 1);
+  SegTable T = make_table(&one, 1);
+  T.argmax_precap = a.argmax_precap ? 1 : 0;
   // no (max, sum exp) pairs: which CTA finishes a row varies from run to run,
   // so the logprobs take the separate pass over the logits (fixed order)
   float2 *parts = nullptr;
@@ -759,7 +762,8 @@ int b1_grid(int64_t n_rows, int num_sms) {
 
 cudaError_t launch_b1(const LaunchArgs &a) {
   const GemvSegment one = {a.w, a.logits, a.n_rows, a.scale, a.cap};
-  const SegTable T = make_table(&one, 1);
+  SegTable T = make_table(&one, 1);
+  T.argmax_precap = a.argmax_precap ? 1 : 0;
   float2 *parts = a.lse_parts ? a.ws.lse_parts : nullptr;   // batch row 0: one pair per CTA
   const int nb = a.k / kBlockWeights;
   if (a.q4) {

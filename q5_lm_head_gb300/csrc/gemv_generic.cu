@@ -59,7 +59,7 @@ template <bool kQ4>
 __global__ void __launch_bounds__(kGemvThreads)
     gemv_generic_kernel(const uint8_t *__restrict__ w, const float *__restrict__ x, int batch,
                         int64_t n_rows, int k, float scale, float cap, float *__restrict__ logits,
-                        unsigned long long *keys, unsigned int *ticket, int32_t *argmax) {
+                        unsigned long long *keys, unsigned int *ticket, int32_t *argmax, int argmax_precap) {
   __shared__ unsigned long long s_best[32];
   const int lane = threadIdx.x & 31;
   const int c = lane >> 3;   // 64-weight group inside a block: sub-blocks 2c and 2c+1
@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(kGemvThreads)
         if (lane == t && b0 + t < batch) {
           const float out = scale_softcap(s, scale, cap);
           logits[static_cast<size_t>(b0 + t) * n_rows + row] = out;
-          if (argmax) atomicMax(&s_best[b0 + t], argmax_key(out, static_cast<uint32_t>(row)));
+          if (argmax)
+            atomicMax(&s_best[b0 + t], argmax_key(argmax_precap ? s * scale : out, static_cast<uint32_t>(row)));
         }
       }
     }
@@ -154,10 +155,12 @@ cudaError_t launch_generic(const LaunchArgs &a) {
   if (blocks > cap_blocks) blocks = cap_blocks;
   if (a.q4)
     gemv_generic_kernel<true><<<static_cast<unsigned>(blocks), kGemvThreads, 0, a.stream>>>(
-        a.w, x, a.batch, a.n_rows, a.k, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax);
+        a.w, x, a.batch, a.n_rows, a.k, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax,
+        a.argmax_precap ? 1 : 0);
   else
     gemv_generic_kernel<false><<<static_cast<unsigned>(blocks), kGemvThreads, 0, a.stream>>>(
-        a.w, x, a.batch, a.n_rows, a.k, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax);
+        a.w, x, a.batch, a.n_rows, a.k, a.scale, a.cap, a.logits, a.ws.keys, a.ws.ticket, a.argmax,
+        a.argmax_precap ? 1 : 0);
   return cudaGetLastError();
 }
 

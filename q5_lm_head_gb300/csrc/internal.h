@@ -43,6 +43,7 @@ struct LaunchArgs {
   cudaStream_t stream;
   bool lse_parts = false;    // batch-1 kernel: also write each CTA's (max, sum exp) pair
   bool q4 = false;           // weights are Q4_K (144-byte blocks) instead of Q5_K
+  bool argmax_precap = false;  // argmax key: raw * scale (before the cap) instead of the returned logit
 };
 
 // One matrix of a grouped batch-1 launch: Q5_K rows `w` ([n_rows][k/256][176]),

@@ -17,6 +17,7 @@
 struct muse_lmhead {
   int device;
   int format;              // MUSE_FORMAT_Q5_K or MUSE_FORMAT_Q4_K
+  int argmax_key;          // MUSE_ARGMAX_CAPPED (default) or MUSE_ARGMAX_PRECAP
   int64_t n_rows;
   int64_t k;
   int max_batch;
@@ -109,6 +110,7 @@ int run_forward(muse_lmhead *h, const float *hidden, int batch, const float *gam
   a.stream = stream;
   a.lse_parts = lse_parts;
   a.q4 = h->format == MUSE_FORMAT_Q4_K;
+  a.argmax_precap = h->argmax_key == MUSE_ARGMAX_PRECAP;
   cudaError_t e;
   switch (choose_path(h, batch)) {
     case Path::B1: e = muse::launch_b1(a); break;
@@ -434,6 +436,13 @@ int muse_lmhead_forward_group_host(muse_lmhead *h, const float *hidden_host, con
       return cuda_fail(e);
   }
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+  return MUSE_OK;
+}
+
+int muse_lmhead_set_argmax_key(muse_lmhead *h, int key) {
+  if (!h) return MUSE_ERR_NULL;
+  if (key != MUSE_ARGMAX_CAPPED && key != MUSE_ARGMAX_PRECAP) return MUSE_ERR_VALUE;
+  h->argmax_key = key;
   return MUSE_OK;
 }
 

@@ -77,6 +77,7 @@ def test_validation_fails_closed_without_cuda(lib):
     assert lib.muse_lmhead_clear_device_status(None, None) == -1
     assert lib.muse_lmhead_selftest_wait_timeout(None, None) == -1
     assert lib.muse_lmhead_path_name(None, 1) is None
+    assert lib.muse_lmhead_set_argmax_key(None, 0) == -1
     lib.muse_lmhead_destroy(None)
 
 
