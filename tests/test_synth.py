@@ -75,3 +75,18 @@ def test_workload_bytes_match_the_roofline_formula():
         assert wl.algorithmic_bytes() == expect, name
     assert synth.WORKLOADS["lmhead_b1"].algorithmic_bytes() == 925_433_088
     assert synth.WORKLOADS["lmhead_q4k_b1"].weight_bytes == 756_467_712      # the Q4_K head of Chapter 20 §20.8
+
+
+def test_group_workload_bytes_and_inputs():
+    """Grouped workloads: every matrix's weights in the group's format, plus one
+    input row, gamma and the outputs; the generated matrices have those sizes."""
+    for name, g in synth.GROUPS.items():
+        bb = {"q5_k": 176, "q4_k": 144}[g.fmt]
+        rows = sum(n for (_, n, _, _, _) in g.segments)
+        assert g.weight_bytes == rows * (g.k // 256) * bb, name
+        assert g.algorithmic_bytes() == g.weight_bytes + g.k * 4 + rows * 4 + (g.k * 4 if g.norm else 0), name
+    ffn = synth.GROUPS["ffn_gate_up_q4k"]
+    assert ffn.weight_bytes == 2 * 19_968 * 26 * 144                   # gate and up, Q4_K
+    assert synth.GROUPS["attn_qkvg"].weight_bytes == (2 * 4096 + 2 * 256) * 26 * 176
+    _, _, ws = synth.group_inputs("attn_qkvg")
+    assert [w.shape for w in ws] == [(n, 26 * 176) for (_, n, _, _, _) in synth.GROUPS["attn_qkvg"].segments]
