@@ -11,13 +11,18 @@
 //
 // A K that is S times a built width (S x 6,656 or S x 4,096 columns) runs the
 // same kernel split along K: CTAs [c*G/S, (c+1)*G/S) of a G-CTA grid stream
-// column chunk c of every row, with chunk c of the input row.  A row tile's S
+// column chunk c of every row, with chunk c of the input row; a tile of a
+// chunk is kRows row-strided copies, one per producer lane.  A row tile's S
 // chunk partials meet in global memory: each chunk CTA stores its rows' sums
 // as it goes; after its last tile the CTA counts in on each of its tiles'
 // counters (a thread per tile: release fence, atomic add, acquire fence when
-// last), and the whole CTA finishes the tiles it arrived last on: the S partials added in chunk order
-// (the same bits whichever CTA that is), then scale, cap and argmax.  No CTA
-// waits on another.
+// last), and the whole CTA finishes the tiles it arrived last on: the S
+// partials added in chunk order (the same bits whichever CTA that is), then
+// scale, cap and argmax.  No CTA waits on another.
+//
+// The argmax ranks the returned logit, or (argmax_precap) scale * raw before
+// the cap; the two orders agree except where the f32 cap rounds distinct
+// values to the same float.
 //
 // Warp roles (one CTA per SM)
 //   * consumer warps: thread (kb, c) owns 64 columns, block kb, sub-blocks 2c
