@@ -165,5 +165,20 @@ def test_group_invalid_arguments_launch_nothing(torch_cuda):
     with mlh.LMHead(1, 512, max_batch=1, device=0) as head512:                            # K with no fused kernel
         assert mlh.muse_lmhead_forward_group(head512.handle, hp, None, 1e-5, [(wp, n, op, 1.0, 0.0)],
                                              None) == -2
+    # the host-buffer form checks the same arguments (its input row and outputs are host memory)
+    h_host = torch.zeros((k,), dtype=torch.float32)
+    o_host = torch.full((n,), 7.0, dtype=torch.float32)
+    hh, oh = h_host.data_ptr(), o_host.data_ptr()
+    with mlh.LMHead(1, k, max_batch=1, device=0) as head:
+        call = mlh.muse_lmhead_forward_group_host
+        assert call(head.handle, hh, None, 1e-5, [], None) == -2                          # no segment
+        assert call(head.handle, None, None, 1e-5, [(wp, n, oh, 1.0, 0.0)], None) == -1   # null hidden
+        assert call(head.handle, hh, None, 1e-5, [(wp, n, None, 1.0, 0.0)], None) == -1   # null out
+        assert call(head.handle, hh, None, 1e-5, [(wp + 8, n, oh, 1.0, 0.0)], None) == -4  # weights alignment
+        assert call(head.handle, hh, None, 1e-5, [(wp, n, oh + 2, 1.0, 0.0)], None) == -4  # out alignment
+        assert call(head.handle, hh, hp, float("inf"), [(wp, n, oh, 1.0, 0.0)], None) == -5  # eps
+    with mlh.LMHead(1, 512, max_batch=1, device=0) as head512:
+        assert mlh.muse_lmhead_forward_group_host(head512.handle, hh, None, 1e-5, [(wp, n, oh, 1.0, 0.0)],
+                                                  None) == -2
     torch.cuda.synchronize()
-    assert torch.all(out == 7.0)                                                          # nothing was written
+    assert torch.all(out == 7.0) and torch.all(o_host == 7.0)                             # nothing was written
