@@ -94,6 +94,36 @@ def test_logprobs_replayed_from_a_cuda_graph(torch_cuda):
             assert torch.equal(x, y)
 
 
+def test_grouped_forward_replayed_from_a_cuda_graph(torch_cuda):
+    """The Q/K/V/gate group captured once and replayed: the segment table is a
+    kernel argument, so every replay writes the same four outputs, bit for bit
+    the eager call's."""
+    import q5_lm_head_gb300 as mlh
+    torch = torch_cuda
+    g = synth.GROUPS["attn_qkvg"]
+    hidden, gamma, ws = synth.group_inputs(g)
+    with mlh.LMHead(1, g.k, max_batch=1, device=0) as head:
+        h, gm = _dev(torch, hidden), _dev(torch, gamma)
+        wd = [_dev(torch, w) for w in ws]
+        ref = head.forward_group(h, [(w, n, sc, cp, None) for w, (_, n, _, sc, cp) in zip(wd, g.segments)], gm)
+        outs = [torch.empty_like(r) for r in ref]
+        segs = [(w, n, sc, cp, o) for w, (_, n, _, sc, cp), o in zip(wd, g.segments, outs)]
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            head.forward_group(h, segs, gm, stream=s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            head.forward_group(h, segs, gm, stream=s)
+        for _ in range(2):
+            for o in outs:
+                o.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            assert all(torch.equal(o, r) for o, r in zip(outs, ref))
+        assert head.device_status() == 0
+
+
 def test_bounded_wait_gives_up_and_reports_without_a_fault(torch_cuda):
     import q5_lm_head_gb300 as mlh
     torch = torch_cuda
