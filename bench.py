@@ -110,6 +110,9 @@ _TC_SRC = ("gemm_tc.cu", "common.cuh", "ptx.cuh", "tc.cuh")
 _PROFILED = {("gemv_b1", "lmhead_b1"): ("gemv_b1_lmhead.md", _B1_SRC),
              ("gemv_b1", "lmhead_q4k_b1"): ("gemv_b1_lmhead_q4k.md", _B1_SRC),
              ("gemm_tc", "lmhead_b8"): ("gemm_tc_lmhead_b8.md", _TC_SRC),
+             ("gemm_tc", "sweep_b2"): ("gemm_tc_sweep_b2.md", _TC_SRC),
+             ("gemm_tc", "dflash_verify_b16"): ("gemm_tc_dflash_verify_b16.md", _TC_SRC),
+             ("gemm_tc", "sweep_b32"): ("gemm_tc_sweep_b32.md", _TC_SRC),
              ("gemv_b1_split", "ffn_down_q4k"): ("gemv_b1_split_ffn_down_q4k.md", _B1_SRC),
              ("gemv_b1_group", "attn_qkvg"): ("gemv_b1_group_attn_qkvg.md", _B1_SRC)}
 
