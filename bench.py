@@ -114,6 +114,12 @@ _PROFILED = {("gemv_b1", "lmhead_b1"): ("gemv_b1_lmhead.md", _B1_SRC),
              ("gemm_tc", "dflash_verify_b16"): ("gemm_tc_dflash_verify_b16.md", _TC_SRC),
              ("gemm_tc", "sweep_b32"): ("gemm_tc_sweep_b32.md", _TC_SRC),
              ("gemv_b1_split", "ffn_down_q4k"): ("gemv_b1_split_ffn_down_q4k.md", _B1_SRC),
+             ("gemm_tc", "lmhead_q4k_b8"): ("gemm_tc_lmhead_q4k_b8.md", _TC_SRC),
+             ("gemv_b1_group", "ffn_gate_up_q4k"): ("gemv_b1_group_ffn_gate_up_q4k.md", _B1_SRC),
+             ("gemv_b1", "tiny"): ("gemv_b1_small_shapes.md", _B1_SRC),
+             ("gemv_b1", "attn_q"): ("gemv_b1_small_shapes.md", _B1_SRC),
+             ("gemv_b1", "attn_k"): ("gemv_b1_small_shapes.md", _B1_SRC),
+             ("gemv_b1", "attn_o"): ("gemv_b1_small_shapes.md", _B1_SRC),
              ("gemv_b1_group", "attn_qkvg"): ("gemv_b1_group_attn_qkvg.md", _B1_SRC)}
 
 
@@ -140,12 +146,13 @@ def _profiled_traffic(kernel_path: str, workload: str):
     for f in ent[1]:
         h.update(kernel_code(f).encode())
     digest, traffic = None, None
+    mine = f"traffic_bytes_per_launch[{workload}]:"     # a summary covering several workloads
     try:
         with open(os.path.join(ROOT, "profiles", ent[0])) as fh:
             for line in fh:
                 if line.startswith("kernel-source:"):
                     digest = line.split()[1]
-                elif line.startswith("traffic_bytes_per_launch:"):
+                elif line.startswith("traffic_bytes_per_launch:") or line.startswith(mine):
                     traffic = int(line.split()[1])
     except OSError:
         return None

@@ -77,3 +77,14 @@ def test_profile_hash_ignores_comments_only():
     raw = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                             "q5_lm_head_gb300", "csrc", "ptx.cuh")).read()
     assert len(code) < len(raw)
+
+
+def test_profiled_traffic_per_workload_lines():
+    """A summary that covers several workloads carries one traffic line per
+    workload; each workload reads its own, and an unprofiled one reads None."""
+    import bench
+    k = bench._profiled_traffic("gemv_b1", "attn_k")
+    q = bench._profiled_traffic("gemv_b1", "attn_q")
+    assert k is not None and q is not None and k != q
+    assert bench._profiled_traffic("gemv_b1", "no_such_workload") is None
+    assert bench._profiled_traffic("gemm_tc", "lmhead_b1") is None
