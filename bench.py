@@ -135,6 +135,21 @@ def kernel_code(name: str) -> str:
     return "\n".join(ln for ln in lines if ln)
 
 
+def _profile_fields(path: str, workload: str):
+    """(kernel-source digest, traffic bytes per launch for `workload`) from an
+    ncu summary: the plain traffic line, or the workload's own line in a
+    summary covering several workloads; None for what is missing."""
+    digest, traffic = None, None
+    mine = f"traffic_bytes_per_launch[{workload}]:"
+    with open(path) as fh:
+        for line in fh:
+            if line.startswith("kernel-source:"):
+                digest = line.split()[1]
+            elif line.startswith("traffic_bytes_per_launch:") or line.startswith(mine):
+                traffic = int(line.split()[1])
+    return digest, traffic
+
+
 def _profiled_traffic(kernel_path: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, or None when there
     is none for this kernel/workload or the kernel source changed since."""
@@ -145,15 +160,8 @@ def _profiled_traffic(kernel_path: str, workload: str):
     h = hashlib.sha256()
     for f in ent[1]:
         h.update(kernel_code(f).encode())
-    digest, traffic = None, None
-    mine = f"traffic_bytes_per_launch[{workload}]:"     # a summary covering several workloads
     try:
-        with open(os.path.join(ROOT, "profiles", ent[0])) as fh:
-            for line in fh:
-                if line.startswith("kernel-source:"):
-                    digest = line.split()[1]
-                elif line.startswith("traffic_bytes_per_launch:") or line.startswith(mine):
-                    traffic = int(line.split()[1])
+        digest, traffic = _profile_fields(os.path.join(ROOT, "profiles", ent[0]), workload)
     except OSError:
         return None
     return traffic if digest and h.hexdigest().startswith(digest) else None

@@ -79,12 +79,18 @@ def test_profile_hash_ignores_comments_only():
     assert len(code) < len(raw)
 
 
-def test_profiled_traffic_per_workload_lines():
+def test_profile_fields_per_workload_lines(tmp_path):
     """A summary that covers several workloads carries one traffic line per
-    workload; each workload reads its own, and an unprofiled one reads None."""
+    workload; each workload reads its own, a plain line serves any workload,
+    and a workload the summary does not name reads None."""
     import bench
-    k = bench._profiled_traffic("gemv_b1", "attn_k")
-    q = bench._profiled_traffic("gemv_b1", "attn_q")
-    assert k is not None and q is not None and k != q
-    assert bench._profiled_traffic("gemv_b1", "no_such_workload") is None
-    assert bench._profiled_traffic("gemm_tc", "lmhead_b1") is None
+    multi = tmp_path / "multi.md"
+    multi.write_text("# title\nkernel-source: 0123abcd  (hash)\n"
+                     "traffic_bytes_per_launch[attn_q]: 111\ntraffic_bytes_per_launch[attn_k]: 222\n")
+    assert bench._profile_fields(str(multi), "attn_q") == ("0123abcd", 111)
+    assert bench._profile_fields(str(multi), "attn_k") == ("0123abcd", 222)
+    assert bench._profile_fields(str(multi), "tiny") == ("0123abcd", None)
+    plain = tmp_path / "plain.md"
+    plain.write_text("kernel-source: feed\ntraffic_bytes_per_launch: 333\n")
+    assert bench._profile_fields(str(plain), "anything") == ("feed", 333)
+    assert bench._profiled_traffic("gemm_tc", "no_such_workload") is None
