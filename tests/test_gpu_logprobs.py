@@ -77,7 +77,7 @@ def test_logprobs_full_lm_head_batch1(torch_cuda):
     _case(torch_cuda, hidden, gamma, wq, wl.n_rows, wl.k, wl.scale, wl.cap, "gemv_b1")
 
 
-@pytest.mark.parametrize("b", [2, 8])
+@pytest.mark.parametrize("b", [2, 8, 32])      # 32 slots: round-robin tiles
 def test_logprobs_tensor_core_path(torch_cuda, b):
     n, k = 20000, 6656
     rng = np.random.default_rng(b)
