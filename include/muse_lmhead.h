@@ -60,7 +60,7 @@ extern "C" {
 
 /* Weight formats (muse_lmhead_init_format). */
 #define MUSE_FORMAT_Q5_K 0   /* 176-byte blocks: the LM head's format (Chapter 20 §20.3) */
-#define MUSE_FORMAT_Q4_K 1   /* 144-byte blocks: the FFN bulk's format, and the 756.5 MB head alternative of §20.8 */
+#define MUSE_FORMAT_Q4_K 1   /* 144-byte blocks: the FFN bulk's format, and the 756.5 MB head alternative of §20.7 */
 
 typedef struct muse_lmhead muse_lmhead;
 

@@ -30,7 +30,7 @@
  * m = (scales[s + 4] >> 4) | (scales[s] >> 6) << 4.
  *
  * Q4_K (the FFN bulk's format, and the 756.5 MB alternative head of Chapter 20
- * §20.8: 144 bytes per 256 weights): the pages give only the block size.
+ * §20.7: 144 bytes per 256 weights): the pages give only the block size.
  * Reading: ggml's block_q4_K — the same fp16 d, fp16 dmin and 12 scale bytes,
  * then 128 bytes of nibbles placed as in Q5_K, no high bits; q in 0..15 and
  * w = d * sc_s * q - dmin * m_s.

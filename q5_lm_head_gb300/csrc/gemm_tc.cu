@@ -1,7 +1,7 @@
 // Batched output stage on the 5th-generation tensor cores (tcgen05), for
 // batches of 2..32 rows: final RMSNorm, Q5_K (or Q4_K) LM-head contraction,
 // scale + soft cap, argmax ("Chapter 20 — Final norm, LM head, and the soft
-// cap", §20.1, §20.3, §20.4, §20.8).  Two launches per forward:
+// cap", §20.1, §20.3, §20.4, §20.7).  Two launches per forward:
 //
 // 1. prep_x_kernel: one CTA per (Q5_K block column kb, package row b).
 //    Normalises hidden row b and writes its part of the block's "activation

@@ -1,6 +1,6 @@
 """GPU parity of Q4_K weights (144-byte blocks: ggml's block_q4_K, the FFN
 bulk's format and the 756.5 MB alternative head of "Chapter 20 — Final norm,
-LM head, and the soft cap" §20.8) against the f64 oracle's own Q4_K parser.
+LM head, and the soft cap" §20.7) against the f64 oracle's own Q4_K parser.
 
 Same bar as Q5_K: |gpu - oracle| <= 2e-3 on every logit, argmax equal where
 the oracle's top-2 gap exceeds 4e-3.  Covers the fused batch-1 kernel (K =

@@ -74,7 +74,7 @@ def test_workload_bytes_match_the_roofline_formula():
         expect = wl.n_rows * nb * bb + wl.batch * wl.k * 4 + wl.batch * wl.n_rows * 4 + (wl.k * 4 if wl.norm else 0)
         assert wl.algorithmic_bytes() == expect, name
     assert synth.WORKLOADS["lmhead_b1"].algorithmic_bytes() == 925_433_088
-    assert synth.WORKLOADS["lmhead_q4k_b1"].weight_bytes == 756_467_712      # the Q4_K head of Chapter 20 §20.8
+    assert synth.WORKLOADS["lmhead_q4k_b1"].weight_bytes == 756_467_712      # the Q4_K head of Chapter 20 §20.7
 
 
 def test_group_workload_bytes_and_inputs():
