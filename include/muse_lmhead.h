@@ -193,26 +193,33 @@ int muse_lmhead_clear_device_status(muse_lmhead *h, void *stream);
 int muse_lmhead_selftest_wait_timeout(muse_lmhead *h, void *stream);
 
 /*
- * Batch-1 forward for callers that cannot allocate device memory at call time
- * (code running during CUDA graph capture, runtimes that reserve all device
- * memory through their own allocator, serving loops that must not risk the
- * implicit synchronisation of cudaMalloc).  No handle: the few bytes of
- * scratch the fused kernel needs (argmax key, completion ticket, status word)
- * live in a fixed 256-byte array inside the library's device memory, which
- * every GPU that loads the library holds until the process exits.  The pages
- * have no counterpart of this call; it is a deployment convenience.
+ * Batch-1 forward for callers that cannot allocate device memory at call time:
+ * runtimes that reserve all device memory up front through their own
+ * allocator and refuse any later cudaMalloc, and serving loops that must not
+ * risk the implicit device synchronisation of cudaMalloc/cudaFree.  No handle:
+ * the few bytes of scratch the fused batch-1 kernel needs (argmax key,
+ * completion ticket, status word) live in a fixed 256-byte array inside the
+ * library's device memory, which every GPU that loads the library holds until
+ * the process exits.  The pages have no counterpart of this call; it is a
+ * deployment convenience.
  *   device   CUDA device the pointers live on (made current for the call).
  *   hidden   [k] f32, one row; gamma/eps/weights/scale/cap/logits/argmax as for
  *            muse_lmhead_forward with batch 1 (logits [n_rows], argmax [1]).
+ *            Weights are Q5_K.  The argmax always ranks the returned (capped)
+ *            logits, MUSE_ARGMAX_CAPPED: there is no handle to select the
+ *            pre-cap key on.
  *   n_rows   1 .. 2^31-1;  k: 4,096 or 6,656 only (the fused kernel's widths),
  *            anything else is rejected with MUSE_ERR_SHAPE before any launch.
  * Calls no cudaMalloc/cudaFree and no allocating library routine.  It clears
- * its scratch with an asynchronous 16-byte memset on `stream`, then launches
- * the kernel.  The first call on a device performs one-time set-up (looks up
- * the scratch array's device address, sets the kernel's shared-memory limit);
- * make that first call before any stream capture.  All calls on a device share
- * the scratch: calls that may overlap on the GPU race on it and must be
- * ordered by the caller (same stream, or events).
+ * the argmax key and ticket with an asynchronous 12-byte memset on `stream`,
+ * then launches the kernel.  The first call on a device performs one-time
+ * set-up (looks up the scratch array's device address, sets the kernel's
+ * shared-memory limit); make that first call before any stream capture.  All
+ * calls on a device share the scratch: calls that may overlap on the GPU race
+ * on it and must be ordered by the caller (same stream, or events).
+ * A bounded wait that gave up inside the kernel (its outputs are then
+ * invalid) sets bit 0 of the scratch's status word, which later calls do not
+ * clear: read it with muse_lmhead_noalloc_device_status.
  */
 int muse_lmhead_forward_b1_noalloc(int device, const float *hidden,
                                    const float *gamma, float eps,
@@ -220,6 +227,16 @@ int muse_lmhead_forward_b1_noalloc(int device, const float *hidden,
                                    int64_t k, float scale, float cap,
                                    float *logits, int32_t *argmax,
                                    void *stream);
+
+/*
+ * Status word of the no-alloc forward on `device` (bit 0: a bounded wait in
+ * one of the kernels gave up since the last read; 0: every such forward ran to
+ * completion).  Waits for the work already queued on `stream` (the stream the
+ * forwards ran on), copies the word into *status and clears it; allocates
+ * nothing.  Forwards still running on other streams race with the read.
+ * The pages have no counterpart.
+ */
+int muse_lmhead_noalloc_device_status(int device, void *stream, uint32_t *status);
 
 /*
  * One matrix of a grouped forward (muse_lmhead_forward_group).

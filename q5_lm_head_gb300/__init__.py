@@ -19,6 +19,7 @@ __all__ = [
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
+    "muse_lmhead_noalloc_device_status",
     "muse_lmhead_forward_group", "muse_lmhead_forward_group_host", "MuseGemvSegment", "MUSE_MAX_SEGMENTS",
     "muse_lmhead_forward_logprobs",
     "muse_lmhead_init_format", "MUSE_FORMAT_Q5_K", "MUSE_FORMAT_Q4_K", "BLOCK_BYTES",
@@ -42,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "muse_lmhead_init", "muse_lmhead_forward", "muse_lmhead_forward_host",
     "muse_lmhead_launches_per_forward", "muse_lmhead_path_name", "muse_lmhead_device_status",
     "muse_lmhead_destroy", "muse_lmhead_status_string", "muse_lmhead_forward_b1_noalloc",
+    "muse_lmhead_noalloc_device_status",
     "muse_lmhead_forward_group", "muse_lmhead_forward_group_host", "muse_lmhead_forward_logprobs",
     "muse_lmhead_init_format",
     "muse_lmhead_clear_device_status", "muse_lmhead_selftest_wait_timeout", "muse_lmhead_set_argmax_key",
@@ -109,6 +111,8 @@ def load_library():
     lib.muse_lmhead_status_string.argtypes = [i32]
     lib.muse_lmhead_forward_b1_noalloc.restype = i32
     lib.muse_lmhead_forward_b1_noalloc.argtypes = [i32, vp, vp, f32, vp, i64, i64, f32, f32, vp, vp, vp]
+    lib.muse_lmhead_noalloc_device_status.restype = i32
+    lib.muse_lmhead_noalloc_device_status.argtypes = [i32, vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.muse_lmhead_clear_device_status.restype = i32
     lib.muse_lmhead_clear_device_status.argtypes = [vp, vp]
     lib.muse_lmhead_selftest_wait_timeout.restype = i32
@@ -185,6 +189,16 @@ def muse_lmhead_forward_b1_noalloc(device: int, hidden: int, gamma: int | None, 
     """Batch-1 forward without a handle that allocates no device memory (see the C header)."""
     return load_library().muse_lmhead_forward_b1_noalloc(device, hidden, gamma, eps, weights, n_rows, k, scale,
                                                          cap, logits, argmax, stream)
+
+
+def muse_lmhead_noalloc_device_status(device: int, stream: int | None) -> int:
+    """Status word of the no-alloc forward on `device`, read after the work
+    queued on `stream` and cleared (see the C header); raises on a failed read."""
+    v = ctypes.c_uint32()
+    st = load_library().muse_lmhead_noalloc_device_status(device, stream, ctypes.byref(v))
+    if st != MUSE_OK:
+        raise MuseError(st, "muse_lmhead_noalloc_device_status")
+    return v.value
 
 
 def muse_lmhead_status_string(status: int) -> str:

@@ -14,6 +14,12 @@
 // it until the process exits; all calls on a device share the array, so two
 // calls that may overlap on the GPU race on it and must be serialised by the
 // caller (one stream, or events).
+//
+// Failure reporting: the kernel ORs a status bit into the array when one of
+// its bounded waits gives up (its logits and argmax are then invalid).  Each
+// forward clears only the argmax key and the ticket, so that bit stays set
+// across later forwards until muse_lmhead_noalloc_device_status reads and
+// clears it.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -29,7 +35,8 @@ namespace {
 constexpr int kScratchBytes = 256;   // stated maximum; the kernel needs 16 of it
 constexpr int kMaxDevices = 64;
 
-// keys (u64) at 0, ticket (u32) at 8, status (u32) at 12
+// keys (u64) at 0, ticket (u32) at 8, status (u32) at kStatusOffset
+constexpr int kStatusOffset = 12;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_setup_mutex;
@@ -92,9 +99,10 @@ extern "C" int muse_lmhead_forward_b1_noalloc(int device, const float *hidden, c
       break;
     }
     if ((st = scratch_for_device(device, &scratch)) != MUSE_OK) break;
-    // key, ticket and status must start at zero; an earlier call leaves them
-    // re-armed, this also covers one that gave up early.
-    if (cudaMemsetAsync(scratch, 0, 16, s) != cudaSuccess) {
+    // key and ticket must start at zero; an earlier call leaves them re-armed,
+    // this also covers one that gave up early.  The status word (bytes 12..15)
+    // is left alone: it keeps a failure until the status call reads it.
+    if (cudaMemsetAsync(scratch, 0, kStatusOffset, s) != cudaSuccess) {
       st = MUSE_ERR_CUDA;
       break;
     }
@@ -113,10 +121,37 @@ extern "C" int muse_lmhead_forward_b1_noalloc(int device, const float *hidden, c
     a.num_sms = sms;
     a.ws.keys = reinterpret_cast<unsigned long long *>(scratch);
     a.ws.ticket = reinterpret_cast<unsigned int *>(scratch + 8);
-    a.ws.status = reinterpret_cast<uint32_t *>(scratch + 12);
+    a.ws.status = reinterpret_cast<uint32_t *>(scratch + kStatusOffset);
     a.ws.x = nullptr;   // the fused kernel normalises in registers and needs no activation buffer
     a.stream = s;
     if (muse::launch_b1(a) != cudaSuccess) st = MUSE_ERR_CUDA;
+  } while (false);
+  if (prev >= 0 && prev != device) cudaSetDevice(prev);
+  return st;
+}
+
+extern "C" int muse_lmhead_noalloc_device_status(int device, void *stream, uint32_t *status) {
+  if (!status) return MUSE_ERR_NULL;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) return MUSE_ERR_CUDA;
+  if (device < 0 || device >= ndev || device >= kMaxDevices) return MUSE_ERR_DEVICE;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return MUSE_ERR_CUDA;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return MUSE_ERR_DEVICE;
+  int st = MUSE_OK;
+  unsigned char *scratch = nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  do {
+    if ((st = scratch_for_device(device, &scratch)) != MUSE_OK) break;
+    // after the caller's earlier work on `stream`: copy the word out, clear it
+    if (cudaMemcpyAsync(&word, scratch + kStatusOffset, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(scratch + kStatusOffset, 0, sizeof(word), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+      st = MUSE_ERR_CUDA;
+      break;
+    }
+    *status = word;
   } while (false);
   if (prev >= 0 && prev != device) cudaSetDevice(prev);
   return st;
