@@ -188,13 +188,14 @@ def replica_aggregate(seconds: float, nbytes: int, device=None):
     return ws * nbytes / seconds / 1e9, seconds
 
 
-def _oracle_rate(wl, hidden, gamma, wq, target_s: float):
+def _oracle_rate(wl, hidden, gamma, wq, target_s: float, threads: int | None = None):
     """Time the oracle, as it stands, on a bounded sample of the workload: the
     first `rows` weight rows (all of them when they fit the time budget), run
-    repeatedly for `target_s` seconds.  Returns (bytes_per_s, rows, reps, cores, secs)."""
+    repeatedly for `target_s` seconds on `threads` threads (all host cores by
+    default).  Returns (bytes_per_s, rows, reps, cores, secs)."""
     import numpy as np
     import oracle
-    cores = oracle.default_threads()
+    cores = threads or oracle.default_threads()
     probe = min(2048, wl.n_rows)
     t0 = time.perf_counter()
     oracle.lmhead(hidden, gamma, wq[:probe], wl.scale, wl.cap, nthreads=cores, fmt=wl.fmt)
@@ -239,7 +240,7 @@ def run_reference(args, wl):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(statistics.median(secs_l) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(wl, 1, "cpu"),
+        "config": _config(wl, ws, _l2_mode(wl)),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -248,6 +249,37 @@ def run_reference(args, wl):
 
 
 METRIC = "Q5_K LM-head forward us and achieved HBM GB/s (% of GB300 peak), batch 1-32"
+
+
+def _big(wl) -> bool:
+    """Whether a workload's bytes exceed L2 enough that every forward streams from HBM."""
+    return wl.algorithmic_bytes() > 2 * L2_BYTES
+
+
+def _l2_mode(wl) -> str:
+    return ("inputs larger than L2 (weights stream from HBM every forward)" if _big(wl) else
+            "L2 flushed before every timed forward (256 MiB write, then a 256 MiB read so that no "
+            "write-back lands in the timed interval; both outside it)")
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or the platform string."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
 
 
 def _config(wl, ws, l2_mode):
@@ -286,10 +318,10 @@ def _e2e(args, wl, head, hidden, w_d, g_d, eps, stream, ws, nbytes):
             "d2h_bytes_per_step": d2h, "us_per_forward": round(secs * 1e6, 2)}
 
 
-def _hold_cycles(steps: int) -> int:
+def _hold_cycles(steps: int, host_s_per_step: float = 0.3e-3, cap_s: float = 2.0) -> int:
     """GPU cycles to sleep while the host enqueues `steps` timed forwards
-    (about 0.3 ms of host work per step, at up to 2.1 GHz)."""
-    return int(min(2.0, 0.3e-3 * (steps + 4)) * 2.1e9)
+    (host_s_per_step of host work per step, at up to 2.1 GHz)."""
+    return int(min(cap_s, host_s_per_step * (steps + 4)) * 2.1e9)
 
 
 def _graph_times(fwd, stream, steps, l2_flush):
@@ -369,11 +401,11 @@ def _e2e_logprobs(args, wl, head, hidden, w_d, g_d, eps, stream, nbytes):
             "d2h_bytes_per_step": wl.batch * (wl.n_rows + 2) * 4, "us_per_forward": round(secs * 1e6, 2)}
 
 
-def _oracle_rate_group(g, hidden, gamma, wqs, target_s: float):
+def _oracle_rate_group(g, hidden, gamma, wqs, target_s: float, threads: int | None = None):
     """The oracle, as it stands, over every matrix of a group, whole passes for
     `target_s` seconds.  Returns (bytes_per_s, rows, reps, cores, secs)."""
     import oracle
-    cores = oracle.default_threads()
+    cores = threads or oracle.default_threads()
     reps = 0
     t0 = time.perf_counter()
     while True:
@@ -384,6 +416,121 @@ def _oracle_rate_group(g, hidden, gamma, wqs, target_s: float):
         if secs >= target_s:
             break
     return g.algorithmic_bytes() * reps / secs, g.n_rows, reps, cores, secs
+
+
+# The whole metric in one run ("batch 1-32" over the five workloads): each entry
+# (workload, what it stands for).  The 202,048-row entries share two weight
+# matrices, generated once: the boosted one (rows 0, 777, 200001) for the
+# batch-1 / batch-8 / DFlash entries and the plain one for the batch sweep.
+SWEEP = (("lmhead_b1", "full LM head, batch 1"), ("lmhead_b8", "full LM head, serving batch 8"),
+         ("sweep_b2", "batch sweep"), ("sweep_b4", "batch sweep"), ("sweep_b8", "batch sweep"),
+         ("sweep_b16", "batch sweep"), ("sweep_b32", "batch sweep"),
+         ("dflash_verify_b16", "DFlash verify batch"),
+         ("tiny", "tiny head, 2,048 rows"), ("attn_q", "attention projection"), ("attn_k", "attention projection"),
+         ("attn_v", "attention projection"), ("attn_o", "attention projection"),
+         ("attn_qkvg", "Q/K/V/gate group, one launch"))
+
+
+def _time_forwards(fwd, stream, n, l2_flush=None):
+    """Per-forward device times (ms) of n forwards enqueued behind a sleep
+    kernel (no interval waits on the host), L2 flushed before each one when a
+    flush is given."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(_hold_cycles(n, 0.1e-3, 1.0))
+        for i in range(n):
+            if l2_flush is not None:
+                l2_flush(i)
+            starts[i].record(stream)
+            fwd()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def run_sweep(args, dev, stream, local, peak, peak_kind, preset=None):
+    """Every workload of the metric on this GPU, one entry each: device time
+    per forward (CUDA events; inputs larger than L2, or L2 flushed before
+    every forward), algorithmic GB/s, fraction of the measured copy peak,
+    kernel path and the clocks sampled while it ran."""
+    import torch
+    import q5k_synth as synth
+    import q5_lm_head_gb300 as mlh
+    eps = synth.RMS_EPS
+    mats = dict(preset or {})          # (weight tag, boosted rows) -> device matrix
+
+    def weights(wl):
+        key = (wl.weight_tag, wl.boost_rows)
+        if key not in mats:
+            mats[key] = torch.from_numpy(synth.weights_for(wl)).to(dev)
+        return mats[key]
+
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    evict = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+
+    def l2_flush(i):
+        flush.fill_(i & 0xFF)
+        evict.sum()
+
+    entries = []
+    for name, what in SWEEP:
+        group = name in synth.GROUPS
+        wl = synth.GROUPS[name] if group else synth.WORKLOADS[name]
+        if group:
+            hidden, gamma, wq = synth.group_inputs(wl)
+            w_d = [torch.from_numpy(w).to(dev) for w in wq]
+            head = mlh.LMHead(1, wl.k, max_batch=1, device=local, fmt=wl.fmt)
+            segs = [(w, n, sc, cp, torch.empty((n,), dtype=torch.float32, device=dev))
+                    for w, (_, n, _, sc, cp) in zip(w_d, wl.segments)]
+            path = "gemv_b1_group"
+        else:
+            hidden, gamma = synth.hidden_for(wl), synth.gamma_for(wl)
+            w_d = weights(wl) if wl.n_rows == synth.VOCAB else torch.from_numpy(synth.weights_for(wl)).to(dev)
+            head = mlh.LMHead(wl.n_rows, wl.k, max_batch=wl.batch, device=local, fmt=wl.fmt)
+            logits = torch.empty((wl.batch, wl.n_rows), dtype=torch.float32, device=dev)
+            amax = torch.empty((wl.batch,), dtype=torch.int32, device=dev) if wl.argmax else None
+            path = head.path_name(wl.batch)
+        h_d = torch.from_numpy(hidden).to(dev)
+        g_d = None if gamma is None else torch.from_numpy(gamma).to(dev)
+
+        def fwd():
+            if group:
+                head.forward_group(h_d, segs, g_d, eps, stream)
+            else:
+                head.forward(h_d, w_d, g_d, eps, wl.scale, wl.cap, wl.argmax, logits, amax, stream)
+
+        big = _big(wl)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fwd()
+        torch.cuda.synchronize()
+        probe = _time_forwards(fwd, stream, 5, None if big else l2_flush)
+        est_ms = statistics.median(probe)
+        # at least args.sweep_seconds of forwards, so the clock sampler sees the GPU under load
+        n = int(max(args.steps, min(20000, args.sweep_seconds * 1e3 / max(est_ms, 1e-3))))
+        if not big:
+            n = min(n, 400)
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.3)
+        per = _time_forwards(fwd, stream, n, None if big else l2_flush)
+        clocks = sampler.stop()
+        ms = (sum(per) / len(per)) if big else statistics.median(per)
+        nbytes = wl.algorithmic_bytes()
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        entries.append({
+            "workload": name, "what": what, "batch": wl.batch, "n_rows": wl.n_rows, "k": wl.k,
+            "weights": "Q5_K" if wl.fmt == "q5_k" else "Q4_K", "kernel_path": path, "forwards": n,
+            "us_per_forward": round(ms * 1e3, 2),
+            "us_stat": "mean of per-forward CUDA-event intervals" if big else
+                       "median of per-forward CUDA-event intervals, L2 flushed before each",
+            "algorithmic_bytes": nbytes, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "logits_per_s": round(wl.batch * wl.n_rows / (ms * 1e-3), 1),
+            "traffic": _profiled_traffic(path, name), "clocks": clocks, "device_status": head.device_status()})
+        head.close()
+    return {"peak_gbs": peak, "peak_source": f"{peak_kind} HBM copy bandwidth", "entries": entries}
 
 
 def run_ours(args, wl):
@@ -428,10 +575,8 @@ def run_ours(args, wl):
             lse_d = torch.empty((wl.batch,), dtype=torch.float32, device=dev)
     h_d = torch.from_numpy(hidden).to(dev)
     g_d = None if gamma is None else torch.from_numpy(gamma).to(dev)
-    big = wl.algorithmic_bytes() > 2 * L2_BYTES
-    l2_mode = ("inputs larger than L2 (weights stream from HBM every forward)" if big else
-               "L2 flushed before every timed forward (256 MiB write, then a 256 MiB read so that no "
-               "write-back lands in the timed interval; both outside it)")
+    big = _big(wl)
+    l2_mode = _l2_mode(wl)
     flush = None if big else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     evict = None if big else torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
 
@@ -530,12 +675,20 @@ def run_ours(args, wl):
     }
     if not group and args.logprobs:
         line["config"]["output"] = "logprobs: log-softmax of the capped logits, plus lse and argmax"
+    if ws == 1 and args.sweep:
+        preset = {} if group else {(wl.weight_tag, wl.boost_rows): w_d}
+        line["sweep"] = run_sweep(args, dev, stream, local, peak, peak_kind, preset)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, rows, reps, cores, secs = (_oracle_rate_group if group else _oracle_rate)(
-            wl, hidden, gamma, wq, args.cpu_seconds)
+        rate_fn = _oracle_rate_group if group else _oracle_rate
+        rate, rows, reps, cores, secs = rate_fn(wl, hidden, gamma, wq, args.cpu_seconds)
+        rate1, rows1, reps1, _, secs1 = rate_fn(wl, hidden, gamma, wq, args.cpu_seconds / 3, threads=1)
         line["cpu_baseline"] = {"value": round(rate / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{rows} of {wl.n_rows} weight rows x batch {wl.batch}, {reps} pass(es), "
-                                          f"{secs:.1f} s wall on {cores} threads"}
+                                          f"{secs:.1f} s wall on {cores} threads",
+                                "single_thread": {"value": round(rate1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                                  "sample": f"{rows1} of {wl.n_rows} weight rows x batch "
+                                                            f"{wl.batch}, {reps1} pass(es), {secs1:.1f} s wall"},
+                                "cpu_model": cpu_model(), "host_cores": os.cpu_count()}
     head.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -557,11 +710,18 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", dest="sweep", action="store_true", default=None,
+                    help="also time every workload of the metric (default: on for the default workload)")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--sweep-seconds", type=float, default=0.8,
+                    help="timed seconds per large sweep entry (lets the clock sampler see each one)")
     ap.add_argument("--rows", type=int, default=0,
                     help="profiling: keep only the first ROWS weight rows of the workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.sweep is None:
+        args.sweep = args.workload == "lmhead_b1" and not args.rows and not args.logprobs
     wl = synth.GROUPS[args.workload] if args.workload in synth.GROUPS else synth.WORKLOADS[args.workload]
     if (args.rows or args.logprobs) and isinstance(wl, synth.GroupWorkload):
         ap.error("--rows and --logprobs apply to single-matrix workloads")
