@@ -56,6 +56,7 @@ def test_forward_replayed_from_a_cuda_graph_matches_eager(torch_cuda, n, k, b, p
         logits = torch.empty_like(ref_l)
         amax = torch.empty_like(ref_a)
         s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())      # a handle's workspace serves one stream at a time
         with torch.cuda.stream(s):                      # one-time set-up happens before the capture
             head.forward(hidden, w, gamma, logits=logits, argmax=amax, stream=s)
         torch.cuda.synchronize()
@@ -81,6 +82,7 @@ def test_logprobs_replayed_from_a_cuda_graph(torch_cuda):
         ref = [t.clone() for t in head.forward_logprobs(h, w, g_)]
         lp, lse, am = torch.empty_like(ref[0]), torch.empty_like(ref[1]), torch.empty_like(ref[2])
         s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())      # a handle's workspace serves one stream at a time
         with torch.cuda.stream(s):
             head.forward_logprobs(h, w, g_, logprobs=lp, lse=lse, argmax=am, stream=s)
         torch.cuda.synchronize()
@@ -109,6 +111,7 @@ def test_grouped_forward_replayed_from_a_cuda_graph(torch_cuda):
         outs = [torch.empty_like(r) for r in ref]
         segs = [(w, n, sc, cp, o) for w, (_, n, _, sc, cp), o in zip(wd, g.segments, outs)]
         s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())      # a handle's workspace serves one stream at a time
         with torch.cuda.stream(s):
             head.forward_group(h, segs, gm, stream=s)
         torch.cuda.synchronize()
