@@ -235,53 +235,73 @@ __device__ __forceinline__ void amin_cols(const RowHdr &h, uint32_t (&o)[8]) {
   o[3] = o[7] = hfma2_u32(magic_pair<2>(h.m47), one, neg1024);
 }
 
-// Columns 32c..32c+31 of A for one row: sub-blocks 2c (low nibbles, built as q)
-// and 2c+1 (high nibbles, built as 2q), as f16 pairs sc_s*q in natural K order;
+// HFMA2 operands of one 32-column chunk: its low nibbles (sub-block 2c) are
+// built as (1024 + q) * sc - 1024 sc, its high nibbles (sub-block 2c+1) as
+// (1024 + 2q) * sc/2 - 512 sc; both exact.  scw holds the chunk's two 6-bit
+// scales as bytes I and I+1.  A single HFMA2 turns the magic pair
+// (1024 + sc_a, 1024 + sc_b) into (sc_a, sc_b / 2), so the constants need
+// three byte permutes and two f16 multiplies, and no conversion.
+struct ChunkK {
+  uint32_t mul_lo, add_lo, mul_hi, add_hi;
+};
+
+constexpr uint32_t kH2OneHalf = 0x38003C00u;      // f16 pair (1, 0.5), low half first
+constexpr uint32_t kH2Neg1024 = 0xE400E400u;      // (-1024, -1024)
+constexpr uint32_t kH2Neg1024_512 = 0xE000E400u;  // (-1024, -512)
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+template <int I>
+__device__ __forceinline__ ChunkK chunk_consts(uint32_t scw) {
+  const uint32_t v = hfma2_u32(magic_pair<I>(scw), kH2OneHalf, kH2Neg1024_512);   // (sc_a, sc_b / 2)
+  ChunkK k;
+  k.mul_lo = __byte_perm(v, 0u, 0x1010u);
+  k.mul_hi = __byte_perm(v, 0u, 0x3232u);
+  k.add_lo = hmul2_u32(k.mul_lo, kH2Neg1024);
+  k.add_hi = hmul2_u32(k.mul_hi, kH2Neg1024);
+  return k;
+}
+
+// Columns 32C..32C+31 of A for one row: sub-blocks 2C (low nibbles, built as q)
+// and 2C+1 (high nibbles, built as 2q), as f16 pairs sc_s*q in natural K order;
 // stored to tensor memory at column `ta` in two 16-column halves.  Q5_K adds
-// each quant's fifth bit from the 32 high-bit bytes; Q4_K has none.
-template <bool kQ4>
-__device__ __forceinline__ void a_chunk_st(const uint8_t *blk, const RowHdr &h, int c, uint32_t ta) {
-  const uint32_t scw = c < 2 ? h.sc03 : h.sc47;
-  const uint32_t sh = 16u * (c & 1);
-  const float sc_lo = static_cast<float>((scw >> sh) & 0xFFu);
-  const float sc_hi = static_cast<float>((scw >> (sh + 8)) & 0xFFu);
+// each quant's fifth bit from the 32 high-bit bytes H (bit 2C of byte l for the
+// low nibble, 2C+1 for the high one); Q4_K has none.
+template <bool kQ4, int C>
+__device__ __forceinline__ void a_chunk_st(const uint8_t *blk, const ChunkK &k, uint32_t ta) {
   constexpr int kQs = kQ4 ? kOffQsQ4 : kOffQs;
-  const uint4 a0 = *reinterpret_cast<const uint4 *>(blk + kQs + 32 * c);
-  const uint4 a1 = *reinterpret_cast<const uint4 *>(blk + kQs + 32 * c + 16);
+  constexpr uint32_t kRot = static_cast<uint32_t>(4 - 2 * C) & 31u;   // bit 2C -> 4, bit 2C+1 -> 5
+  const uint4 a0 = *reinterpret_cast<const uint4 *>(blk + kQs + 32 * C);
+  const uint4 a1 = *reinterpret_cast<const uint4 *>(blk + kQs + 32 * C + 16);
   const uint32_t A[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-  uint32_t H[8] = {};
+  uint32_t Hr[8] = {};
   if constexpr (!kQ4) {
     const uint4 h0 = *reinterpret_cast<const uint4 *>(blk + kOffQh);
     const uint4 h1 = *reinterpret_cast<const uint4 *>(blk + kOffQh + 16);
-    H[0] = h0.x; H[1] = h0.y; H[2] = h0.z; H[3] = h0.w;
-    H[4] = h1.x; H[5] = h1.y; H[6] = h1.z; H[7] = h1.w;
-    const uint32_t rot = static_cast<uint32_t>(4 - 2 * c) & 31u;   // bit 2c -> 4, bit 2c+1 -> 5
+    const uint32_t H[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) H[i] = rotl32(H[i], rot);
+    for (int i = 0; i < 8; ++i) Hr[i] = kRot == 0 ? H[i] : rotl32(H[i], kRot);
   }
   uint32_t o[16];
-  {
-    const uint32_t mul = h2_bits(sc_lo), add = h2_bits(-1024.0f * sc_lo);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t q = A[i] & 0x0F0F0F0Fu;                                        // q, positions 4i..4i+3
-      if constexpr (!kQ4) q |= H[i] & 0x10101010u;
-      o[2 * i] = hfma2_u32(magic_pair<0>(q), mul, add);
-      o[2 * i + 1] = hfma2_u32(magic_pair<2>(q), mul, add);
-    }
-    tc::st_32x32b_x16(ta, o);
+  for (int i = 0; i < 8; ++i) {
+    uint32_t q = A[i] & 0x0F0F0F0Fu;                                          // q, positions 4i..4i+3
+    if constexpr (!kQ4) q |= Hr[i] & 0x10101010u;
+    o[2 * i] = hfma2_u32(magic_pair<0>(q), k.mul_lo, k.add_lo);
+    o[2 * i + 1] = hfma2_u32(magic_pair<2>(q), k.mul_lo, k.add_lo);
   }
-  {
-    const uint32_t mul = h2_bits(0.5f * sc_hi), add = h2_bits(-512.0f * sc_hi);
+  tc::st_32x32b_x16(ta, o);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t q = (A[i] >> 3) & 0x1E1E1E1Eu;                                 // 2q
-      if constexpr (!kQ4) q |= H[i] & 0x20202020u;
-      o[2 * i] = hfma2_u32(magic_pair<0>(q), mul, add);
-      o[2 * i + 1] = hfma2_u32(magic_pair<2>(q), mul, add);
-    }
-    tc::st_32x32b_x16(ta + 16, o);
+  for (int i = 0; i < 8; ++i) {
+    uint32_t q = (A[i] >> 3) & 0x1E1E1E1Eu;                                   // 2q
+    if constexpr (!kQ4) q |= Hr[i] & 0x20202020u;
+    o[2 * i] = hfma2_u32(magic_pair<0>(q), k.mul_hi, k.add_hi);
+    o[2 * i + 1] = hfma2_u32(magic_pair<2>(q), k.mul_hi, k.add_hi);
   }
+  tc::st_32x32b_x16(ta + 16, o);
 }
 
 __device__ __forceinline__ void ld_x4(uint32_t ta, uint32_t (&v)[4]) {
@@ -633,8 +653,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      a_chunk_st<kQ4>(blk, hd, 2 * hf, ta);
-      a_chunk_st<kQ4>(blk, hd, 2 * hf + 1, ta + 32);
+      if (hf == 0) {
+        a_chunk_st<kQ4, 0>(blk, chunk_consts<0>(hd.sc03), ta);
+        a_chunk_st<kQ4, 1>(blk, chunk_consts<2>(hd.sc03), ta + 32);
+      } else {
+        a_chunk_st<kQ4, 2>(blk, chunk_consts<0>(hd.sc47), ta);
+        a_chunk_st<kQ4, 3>(blk, chunk_consts<2>(hd.sc47), ta + 32);
+      }
       if (hf == 0) {
         uint32_t am[8];
         amin_cols(hd, am);
