@@ -53,13 +53,16 @@
 //     release the stage, and only then is it armed with its first weight tile.
 //
 // Arithmetic of a consumer thread (exact up to f32 rounding of the last steps)
-//   Its 64 normalised activations x_j are written as x_j = sigma * xi_j with a
-//   per-thread sigma = max|x| / 4194300 and integers |xi_j| < 2^22, stored as
-//   three byte planes xi = 65536*x2 + 256*x1 + x0 (x2 signed, x1 and x0 unsigned).
+//   Its 64 normalised activations x_j = r * h_j * gamma_j are written as
+//   x_j = r * sigma * xi_j with integers |xi_j| < 2^22 and a per-unit power of
+//   two sigma (the largest |h * gamma| of the unit's 64 columns lies in
+//   [2^21, 2^22) sigma, so the scaling is exact and needs no division), stored
+//   as three byte planes xi = 65536*x2 + 256*x1 + x0 (x2 signed, x1 and x0
+//   unsigned).  The RMS factor r only scales sigma and the column sums.
 //   For each sub-block s, sum_j q_j xi_j is built with dp4a on four 5-bit quants
 //   per word (low nibble | high bit << 4; high nibbles are taken as 2q so no
 //   extra shift is needed) against each plane, in exact integer arithmetic.
-//   Then raw += d * sigma * sum_s sc_s * (that) - dmin * sum_s m_s * sum_j x_j,
+//   Then raw += d * r * sigma * sum_s sc_s * (that) - dmin * sum_s m_s * sum_j x_j,
 //   which is sum_j (d*sc_s*q_j - dmin*m_s) x_j up to rounding (§20.1 matvec
 //   with the Q5_K weight w = d*sc*q - dmin*m).
 #include <atomic>
@@ -75,7 +78,6 @@ namespace {
 constexpr int kRows = 12;           // weight rows per pipeline stage (one 1-D bulk copy)
 constexpr int kStreams = 4;         // row teams of consumer threads
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // opt-in limit minus static shared memory
-constexpr float kQuantMax = 4194300.0f;   // |xi| stays below 2^22 after rounding
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 
 // NB blocks per row; kQ4: Q4_K blocks (144 bytes, nibbles only) instead of Q5_K.
@@ -93,26 +95,25 @@ struct B1Cfg {
   static constexpr int kRowBytes = NB * kBB;
   static constexpr int kStageBytes = kRows * kRowBytes;
   static constexpr int kSlotBytes = kRows * NB * 4;         // one partial per (row, block)
-  static constexpr int kFixedBytes = 512;                   // barriers + scratch
-  static constexpr int kStagesFit = (kMaxSmem - kFixedBytes - 2 * kSlotBytes) / (kStageBytes + kSlotBytes);
+  static constexpr int kFixedBytes = 640;                   // barriers, scratch, tile table, stage row counts
+  static constexpr int kStagesFit =
+      (kMaxSmem - kFixedBytes - 4 * 8 * kUnits - 2 * kSlotBytes) / (kStageBytes + kSlotBytes);
   static constexpr int kStages = (kStagesFit > 8 ? 8 : kStagesFit) & ~1;   // even: one parity per producer
   static_assert(kStages >= 4, "need at least double buffering per producer");
   static constexpr int kSlots = kStages + 2;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kSlots * kSlotBytes + kFixedBytes;
+  static constexpr int kExBytes = kUnits * 4 * 8;              // prologue: (max, sum) of every quarter
+  static constexpr int kSmemBytes = kStages * kStageBytes + kSlots * kSlotBytes + kFixedBytes + kExBytes;
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
   // the prologue stages hidden (and gamma) in the last stage, or gamma in the one
   // before when both do not fit one stage
   static_assert(NB * kBlockWeights * 4 <= kStageBytes, "hidden fits one stage");
   static constexpr int kHoldStages = 2 * NB * kBlockWeights * 4 <= kStageBytes ? 1 : 2;
   static constexpr int kEarlyTiles = kStages - kHoldStages;   // armed before the CTA-wide barrier
-  // after the activations are loaded the staging stage holds, per unit, the
-  // four (amax, sum) pairs of its quarters and its plane words (p2, p1, p0:
-  // 16 words each, padded to 52 so the units' rows fall on distinct banks)
+  // after the activations are loaded the staging stage holds, per unit, its
+  // plane words (p2, p1, p0: 16 words each, padded to 52 so the units' rows
+  // fall on distinct banks)
   static constexpr int kPlaneStride = 52;
-  static constexpr int kExBytes = kUnits * 4 * 8;
-  static constexpr int kPlaneOffset = 4096;
-  static_assert(kExBytes <= kPlaneOffset, "exchange area");
-  static_assert(kPlaneOffset + kUnits * kPlaneStride * 4 <= kStageBytes, "plane area");
+  static_assert(kUnits * kPlaneStride * 4 <= kStageBytes, "plane area");
 };
 
 __device__ __forceinline__ uint32_t rotl32(uint32_t v, uint32_t s) { return __funnelshift_l(v, v, s); }
@@ -140,6 +141,16 @@ __device__ __forceinline__ void quantize_chunk(const float (&x)[4], float inv, u
   // high byte h + 0x40 in 0..127 -> h: flip bit 6, then copy bit 6 into bit 7
   const uint32_t h = __byte_perm(u01, u23, 0x5410) ^ 0x40404040u;
   w2 = h | ((h & 0x40404040u) << 1);
+}
+
+// Biased exponent of the power-of-two quantisation factor inv of a unit whose
+// largest |value| is m > 0 (finite): for m in [2^(E-127), 2^(E-126)), E its
+// biased exponent, inv = 2^(148-E), so m * inv lies in [2^21, 2^22) and every
+// |xi| < 2^22; x * inv is exact.  Capped at 252 (m below 2^-104 gets a coarser
+// step) so that 1 / (2 inv) = 2^(126-eb) stays a normal float.
+__device__ __forceinline__ int pow2_step_exponent(float m) {
+  const int e = static_cast<int>(__float_as_uint(m) >> 23);
+  return 275 - e < 252 ? 275 - e : 252;
 }
 
 // Per-thread constants that select this thread's sub-blocks 2c and 2c+1.
@@ -224,6 +235,12 @@ struct SegTable {
   int64_t tile_end[kMaxSegments];
   int n;
   int argmax_precap;   // argmax key: raw * scale (before the cap) instead of the returned logit
+  // Balanced tiles (one small matrix): CTA c takes rows_per (+1 for c < extra)
+  // consecutive rows, cut into tiles of kRows rows and one shorter last tile.
+  // Otherwise CTA c takes the kRows-row tiles c, c + grid, ...
+  int balanced;
+  int rows_per, extra;
+  int grid;            // CTAs of the launch
 };
 
 // Where global tile `tile` lives: its matrix, its first row there and its rows.
@@ -278,27 +295,58 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
   unsigned long long *s_best = reinterpret_cast<unsigned long long *>(s_red + 32);
   volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(s_best + 1);
   float2 *s_ms = reinterpret_cast<float2 *>(s_best + 2);                   // [2] producers' (max, sum exp)
+  float2 *s_ex = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(full) + C::kFixedBytes);   // [kUnits][4]
+  static_assert(16 * C::kStages + 176 <= 512, "fixed area: barriers and scratch");
+  // rows of the tile in each stage, written by whoever arms the stage before its
+  // expect-tx arrive (release) and read by the consumers after the stage's
+  // completion (acquire): the consumers never look the tile up themselves
+  int *s_rows = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(full) + 512);   // [kStages]
+  static_assert(512 + 4 * C::kStages <= C::kFixedBytes, "stage row counts");
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int64_t n_tiles = segs.tile_end[segs.n - 1];
   // This CTA's tiles: tile_first, tile_first + tile_step, ... of its chunk
-  // (one chunk, all CTAs, unless split along K).
-  int chunk = 0;
-  int64_t tile_first = blockIdx.x, tile_step = gridDim.x;
+  // (one chunk, all CTAs, unless split along K).  32-bit arithmetic: the grid
+  // is at most the SM count and a tile count fits easily.
+  int chunk = 0, tile_first = static_cast<int>(blockIdx.x), tile_step = static_cast<int>(gridDim.x);
   if constexpr (kSplit) {
-    chunk = static_cast<int>(((static_cast<int64_t>(blockIdx.x) + 1) * n_chunks - 1) / gridDim.x);
-    const int64_t lo = static_cast<int64_t>(chunk) * gridDim.x / n_chunks;
-    tile_first = blockIdx.x - lo;
-    tile_step = (static_cast<int64_t>(chunk) + 1) * gridDim.x / n_chunks - lo;
+    const int g = static_cast<int>(gridDim.x), bx = static_cast<int>(blockIdx.x);
+    chunk = ((bx + 1) * n_chunks - 1) / g;
+    const int lo = chunk * g / n_chunks;
+    tile_first = bx - lo;
+    tile_step = (chunk + 1) * g / n_chunks - lo;
   }
-  const int my_tiles = tile_first < n_tiles ? static_cast<int>((n_tiles - 1 - tile_first) / tile_step) + 1 : 0;
+  const float *x_src = hidden + static_cast<size_t>(chunk) * K;           // the chunk's input columns
+  const float *g_src = gamma ? gamma + static_cast<size_t>(chunk) * K : nullptr;
+  if (tid == 0) {
+    // The hidden row and gamma go out first, ahead of everything else: the
+    // prologue waits on them, and a launch this small is a chain of latencies.
+    ptx::mbar_init(pro_full, 1);
+    ptx::fence_barrier_init();
+    const uint32_t row_bytes = static_cast<uint32_t>(K) * 4u;
+    ptx::mbar_arrive_expect_tx(pro_full, gamma ? 2u * row_bytes : row_bytes);
+    ptx::bulk_g2s_nohint(const_cast<float *>(s_hidden), x_src, row_bytes, pro_full);
+    if (gamma) ptx::bulk_g2s_nohint(const_cast<float *>(s_gamma), g_src, row_bytes, pro_full);
+  }
+  const int n_tiles = static_cast<int>(segs.tile_end[segs.n - 1]);
+  int my_tiles = tile_first < n_tiles ? (n_tiles - 1 - tile_first) / tile_step + 1 : 0;
+  // balanced share: rows [b_first, b_first + b_rows) of matrix 0
+  const int bx = static_cast<int>(blockIdx.x);
+  const int b_first = bx * segs.rows_per + (bx < segs.extra ? bx : segs.extra);
+  const int b_rows = segs.rows_per + (bx < segs.extra ? 1 : 0);
+  if (segs.balanced) my_tiles = (b_rows + kRows - 1) / kRows;
+  // local tile j of this CTA: its matrix, first row and rows
+  auto tile_at = [&](int j) -> TileLoc {
+    if (segs.balanced) {
+      const int left = b_rows - j * kRows;
+      return TileLoc{0, b_first + j * kRows, left < kRows ? left : kRows};
+    }
+    return locate<kGroup>(segs, tile_first + static_cast<int64_t>(j) * tile_step);
+  };
   // weight tiles armed by the barrier thread before the CTA-wide barrier; a
   // split chunk's tiles are row-strided (one copy per row), so its producers
   // arm them all, a row per lane
   constexpr int kEarly = kSplit ? 0 : C::kEarlyTiles;
-  const float *x_src = hidden + static_cast<size_t>(chunk) * K;           // the chunk's input columns
-  const float *g_src = gamma ? gamma + static_cast<size_t>(chunk) * K : nullptr;
   // the rows of local tile j: one bulk copy, or one per row of a split chunk
   // (rows n_chunks * kRowBytes apart); lanes l0, l0 + ls, ... issue them
   auto issue_tile = [&](const TileLoc &L, int st, uint64_t policy, int l0, int ls) {
@@ -319,26 +367,17 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], C::kConsumerWarps);
     }
-    ptx::mbar_init(pro_full, 1);
     ptx::mbar_init(pro_done, C::kConsumerWarps);
     *s_best = 0ull;
     *s_abort = 0u;
     ptx::fence_barrier_init();
-    // The copies start here, from code this thread is already running: first
-    // the hidden row and gamma (the prologue waits on them), then the first
-    // weight tiles (the stages that hold no prologue data); the producers arm
-    // the later tiles.
-    {
-      const uint32_t row_bytes = static_cast<uint32_t>(K) * 4u;
-      ptx::mbar_arrive_expect_tx(pro_full, gamma ? 2u * row_bytes : row_bytes);
-      ptx::bulk_g2s_nohint(const_cast<float *>(s_hidden), x_src, row_bytes, pro_full);
-      if (gamma) ptx::bulk_g2s_nohint(const_cast<float *>(s_gamma), g_src, row_bytes, pro_full);
-    }
+    // Then the first weight tiles (the stages that hold no prologue data),
+    // from code this thread is already running; the producers arm the later
+    // tiles.
     const uint64_t policy = ptx::policy_evict_first();
-    for (int j = 0; j < kEarly; ++j) {
-      const int64_t tile = tile_first + static_cast<int64_t>(j) * tile_step;
-      if (tile >= n_tiles) break;
-      const TileLoc L = locate<kGroup>(segs, tile);
+    for (int j = 0; j < kEarly && j < my_tiles; ++j) {
+      const TileLoc L = tile_at(j);
+      s_rows[j] = L.rows;
       ptx::mbar_arrive_expect_tx(&full[j], static_cast<uint32_t>(L.rows * C::kRowBytes));
       issue_tile(L, j, policy, 0, 1);
     }
@@ -364,8 +403,7 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     MaxSum ms = ms_empty();                     // log-softmax normaliser of this lane's rows
     // finish the rows of local tile j (its consumers have released its stage)
     auto finish = [&](int j) {
-      const int64_t tile = tile_first + static_cast<int64_t>(j) * tile_step;
-      const TileLoc L = locate<kGroup>(segs, tile);
+      const TileLoc L = tile_at(j);
       const GemvSegment &G = segs.seg[L.s];
       const float *pr = slots + (j % C::kSlots) * (C::kSlotBytes / 4) + er * NB;
       float sacc = 0.0f;
@@ -418,15 +456,19 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
         }
       }
       if constexpr (kSplit) {                  // every tile, one row per lane
-        const TileLoc L = locate<kGroup>(segs, tile_first + static_cast<int64_t>(j) * tile_step);
+        const TileLoc L = tile_at(j);
         const int st = j % C::kStages;
-        if (lane == 0) ptx::mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(L.rows * C::kRowBytes));
+        if (lane == 0) {
+          s_rows[st] = L.rows;
+          ptx::mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(L.rows * C::kRowBytes));
+        }
         __syncwarp();
         issue_tile(L, st, policy, lane, 32);
       } else if (lane == 0 && j >= C::kEarlyTiles) {   // the first ones went out with the barrier set-up
-        const TileLoc L = locate<kGroup>(segs, blockIdx.x + static_cast<int64_t>(j) * gridDim.x);
+        const TileLoc L = tile_at(j);
         const uint32_t bytes = static_cast<uint32_t>(L.rows * C::kRowBytes);
         const int st = j % C::kStages;
+        s_rows[st] = L.rows;
         ptx::mbar_arrive_expect_tx(&full[st], bytes);
         ptx::bulk_g2s(stages + st * C::kStageBytes, segs.seg[L.s].w + L.r0 * C::kRowBytes, bytes, &full[st],
                       policy);
@@ -461,44 +503,18 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     const int u = tid % C::kUnits;
     const int kb = u >> 2, c = u & 3;
 
-    // Prologue: the hidden row (and gamma) arrive in the last stage.
+    // Prologue: the hidden row (and gamma) arrive in the last stage.  Unit u's
+    // 64 columns are quantised by its four threads (one per stream), a quarter
+    // (16 columns) each: quarter q = (stream + u) mod 4, chunk order rotated by
+    // (u / 2) mod 4, which puts the eight lanes of every quarter-warp on
+    // distinct shared-memory banks.  The quantisation step is a power of two
+    // fixed by the largest |h * gamma| of the unit, so it needs neither the RMS
+    // factor r nor a division: r only scales sigma and the column sums.  Two
+    // barriers: after the first every consumer has read the staged row and
+    // posted its sum of squares and its quarter's (max, sum); after the second
+    // the unit's plane words are in shared memory.
     bool pro_ok = __all_sync(0xffffffffu, ptx::mbar_wait(pro_full, 0));
     if (!pro_ok && lane == 0) fail();
-    // Final RMSNorm: every CTA recomputes r from the staged row.
-    float r = 1.0f;
-    if (gamma) {
-      float ss = 0.0f;
-      if constexpr (kSplit) {                   // the whole row's mean square (all chunks), from global memory
-        const int kt = K * n_chunks;
-        for (int j = tid * 4; j < kt; j += C::kConsumers * 4) {
-          const float4 v = __ldg(reinterpret_cast<const float4 *>(hidden + j));
-          ss = fmaf(v.x, v.x, ss);
-          ss = fmaf(v.y, v.y, ss);
-          ss = fmaf(v.z, v.z, ss);
-          ss = fmaf(v.w, v.w, ss);
-        }
-      } else {
-        for (int j = tid * 4; j < K; j += C::kConsumers * 4) {
-          const float4 v = *reinterpret_cast<const float4 *>(s_hidden + j);
-          ss = fmaf(v.x, v.x, ss);
-          ss = fmaf(v.y, v.y, ss);
-          ss = fmaf(v.z, v.z, ss);
-          ss = fmaf(v.w, v.w, ss);
-        }
-      }
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) s_red[warp] = ss;
-      ptx::named_bar_sync(1, C::kConsumers);
-      float tot = 0.0f;
-      for (int i = 0; i < C::kConsumerWarps; ++i) tot += s_red[i];
-      r = 1.0f / sqrtf(tot / static_cast<float>(kSplit ? K * n_chunks : K) + eps);
-    }
-    // This thread's activations: unit u = (kb, c) covers 64 columns, sub-block
-    // 2c (x_lo, natural chunks 0..7 of four columns) and 2c+1 (x_hi, chunks
-    // 8..15).  The unit's four threads (one per stream) each load and quantise
-    // one quarter (four chunks): quarter q = (stream + u) mod 4, chunk order
-    // rotated by (u / 2) mod 4, which puts the eight lanes of every
-    // quarter-warp on distinct shared-memory banks.
     XPlanes xl, xh;
     float sx_lo, sx_hi, sigma_half;
     {
@@ -506,33 +522,64 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
       const int rot = (u >> 1) & 3;
       const int base = kb * kBlockWeights + 64 * c + 16 * q;
       float xv[4][4];
-      float amax = 0.0f, psum = 0.0f;
+      float amax = 0.0f, psum = 0.0f, ss = 0.0f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int off = base + 4 * ((i + rot) & 3);
         float4 h = *reinterpret_cast<const float4 *>(s_hidden + off);
         if (gamma) {
+          if constexpr (!kSplit) {              // the quarters of all threads tile the row once
+            ss = fmaf(h.x, h.x, ss);
+            ss = fmaf(h.y, h.y, ss);
+            ss = fmaf(h.z, h.z, ss);
+            ss = fmaf(h.w, h.w, ss);
+          }
           const float4 g = *reinterpret_cast<const float4 *>(s_gamma + off);
-          h = make_float4(h.x * r * g.x, h.y * r * g.y, h.z * r * g.z, h.w * r * g.w);
+          h = make_float4(h.x * g.x, h.y * g.y, h.z * g.z, h.w * g.w);
         }
         xv[i][0] = h.x; xv[i][1] = h.y; xv[i][2] = h.z; xv[i][3] = h.w;
         psum += (h.x + h.y) + (h.z + h.w);
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
       }
-      // every consumer has read the staged row: its space is reused from here
-      ptx::named_bar_sync(1, C::kConsumers);
-      float2 *s_ex = reinterpret_cast<float2 *>(stages + (C::kStages - 1) * C::kStageBytes);
-      uint32_t *s_pl = reinterpret_cast<uint32_t *>(stages + (C::kStages - 1) * C::kStageBytes + C::kPlaneOffset) +
-                       u * C::kPlaneStride;
+      if constexpr (kSplit) {                   // the whole row's mean square (all chunks), from global memory
+        if (gamma) {
+          const int kt = K * n_chunks;
+          for (int j = tid * 4; j < kt; j += C::kConsumers * 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(hidden + j));
+            ss = fmaf(v.x, v.x, ss);
+            ss = fmaf(v.y, v.y, ss);
+            ss = fmaf(v.z, v.z, ss);
+            ss = fmaf(v.w, v.w, ss);
+          }
+        }
+      }
+      if (gamma) {
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) s_red[warp] = ss;
+      }
       s_ex[u * 4 + q] = make_float2(amax, psum);
       ptx::named_bar_sync(1, C::kConsumers);
+      // Final RMSNorm factor r = 1 / sqrt(mean(h^2) + eps), the warps' sums
+      // added in warp order (every CTA the same bits).
+      float r = 1.0f;
+      if (gamma) {
+        float tot = 0.0f;
+        for (int i = 0; i < C::kConsumerWarps; ++i) tot += s_red[i];
+        r = rsqrtf(fmaf(tot, 1.0f / static_cast<float>(kSplit ? K * n_chunks : K), eps));
+      }
       const float4 e01 = *reinterpret_cast<const float4 *>(s_ex + u * 4);
       const float4 e23 = *reinterpret_cast<const float4 *>(s_ex + u * 4 + 2);
       const float umax = fmaxf(fmaxf(e01.x, e01.z), fmaxf(e23.x, e23.z));
-      sx_lo = e01.y + e01.w;                 // quarters 0 and 1
-      sx_hi = e23.y + e23.w;                 // quarters 2 and 3
-      const float inv = umax > 0.0f ? kQuantMax / umax : 0.0f;
-      sigma_half = umax > 0.0f ? 0.5f / inv : 0.0f;   // the 1/2 undoes the 2q form of the high nibbles
+      sx_lo = r * (e01.y + e01.w);             // quarters 0 and 1
+      sx_hi = r * (e23.y + e23.w);             // quarters 2 and 3
+      float inv = 0.0f;
+      sigma_half = 0.0f;
+      if (umax > 0.0f) {
+        const int eb = pow2_step_exponent(umax);
+        inv = __uint_as_float(static_cast<uint32_t>(eb) << 23);
+        sigma_half = r * __uint_as_float(static_cast<uint32_t>(253 - eb) << 23);   // the 1/2 undoes the 2q form
+      }
+      uint32_t *s_pl = reinterpret_cast<uint32_t *>(stages + (C::kStages - 1) * C::kStageBytes) + u * C::kPlaneStride;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         uint32_t w2, w1, w0;
@@ -571,14 +618,14 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
 
     int st = 0, ps = 0;
     uint32_t ph = 0;                           // round parity of the stage ring
-    for (int64_t tile = tile_first; tile < n_tiles && pro_ok; tile += tile_step) {
+    for (int j = 0; j < my_tiles && pro_ok; ++j) {
       // every exit decision is taken by the whole warp (the loop body shuffles)
       if (__any_sync(0xffffffffu, *s_abort != 0u)) break;
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full[st], ph))) {
         if (lane == 0) fail();
         break;
       }
-      const int rows = locate<kGroup>(segs, tile).rows;
+      const int rows = s_rows[st];
       float *slot = slots + ps * (C::kSlotBytes / 4) + kb;
       const uint8_t *sbase = stages + st * C::kStageBytes + kb * C::kBB;
       float pv[kRows / kStreams];
@@ -696,22 +743,46 @@ cudaError_t launch_b1_nb(const float *hidden, const float *gamma, float eps, con
   const int64_t n_tiles = T.tile_end[T.n - 1];
   // split along K: n_chunks row tiles per tile of rows, at least one CTA per chunk
   const int64_t units = n_tiles * n_chunks;
-  const int64_t grid = units < num_sms ? units : num_sms;
+  const int64_t grid = kSplit ? (units < num_sms ? units : num_sms) : T.grid;
   if (kSplit && (n_chunks < 2 || grid < n_chunks || !split_part || !split_cnt)) return cudaErrorInvalidValue;
   gemv_b1_kernel<NB, kGroup, kQ4, kSplit><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
       hidden, gamma, eps, T, keys, ticket, argmax, status, lse_parts, n_chunks, split_part, split_cnt);
   return cudaGetLastError();
 }
 
-SegTable make_table(const GemvSegment *segs, int n) {
+// The matrices' tile table and how the CTAs share the tiles.  Round-robin
+// kRows-row tiles stream the whole GPU through one contiguous stretch of the
+// weights, the right order for large matrices.  A small launch is a chain of
+// latencies in which the CTA with the most work sets the time: for a single
+// matrix an even share of rows per CTA (balanced mode) is taken when it lowers
+// the most row rounds any CTA runs (a round = one row per consumer stream; a
+// share of m rows takes ceil(m / 4) rounds) and a share is at most
+// kMaxBalancedRows rows.
+constexpr int64_t kMaxBalancedRows = 12 * kRows;
+
+SegTable make_table(const GemvSegment *segs, int n, int num_sms, bool allow_balanced) {
   SegTable T = {};
-  int64_t end = 0;
+  int64_t end = 0, rows = 0;
   for (int i = 0; i < n; ++i) {
     T.seg[i] = segs[i];
     end += (segs[i].n_rows + kRows - 1) / kRows;
     T.tile_end[i] = end;
+    rows += segs[i].n_rows;
   }
   T.n = n;
+  T.grid = static_cast<int>(end < num_sms ? end : num_sms);
+  if (allow_balanced && n == 1 && rows > 0 && num_sms > 0) {
+    const int64_t rr_rounds = (end + num_sms - 1) / num_sms * (kRows / kStreams);
+    const int64_t grid = rows < num_sms ? rows : num_sms;
+    const int64_t share = (rows + grid - 1) / grid;
+    const int64_t rounds = (share + kStreams - 1) / kStreams;
+    if (share <= kMaxBalancedRows && rounds < rr_rounds) {
+      T.balanced = 1;
+      T.grid = static_cast<int>(grid);
+      T.rows_per = static_cast<int>(rows / grid);
+      T.extra = static_cast<int>(rows % grid);
+    }
+  }
   return T;
 }
 
@@ -741,7 +812,7 @@ cudaError_t launch_b1_split(const LaunchArgs &a) {
   split_shape(a.k, cnb, s);
   if (b1_split_chunks(a.k) == 0 || a.num_sms < s) return cudaErrorInvalidValue;
   const GemvSegment one = {a.w, a.logits, a.n_rows, a.scale, a.cap};
-  SegTable T = make_table(&one, 1);
+  SegTable T = make_table(&one, 1, a.num_sms, false);
   T.argmax_precap = a.argmax_precap ? 1 : 0;
   // no (max, sum exp) pairs: which CTA finishes a row varies from run to run,
   // so the logprobs take the separate pass over the logits (fixed order)
@@ -761,13 +832,13 @@ cudaError_t launch_b1_split(const LaunchArgs &a) {
 }
 
 int b1_grid(int64_t n_rows, int num_sms) {
-  const int64_t n_tiles = (n_rows + kRows - 1) / kRows;
-  return static_cast<int>(n_tiles < num_sms ? n_tiles : num_sms);
+  const GemvSegment one = {nullptr, nullptr, n_rows, 1.0f, 0.0f};
+  return make_table(&one, 1, num_sms, true).grid;
 }
 
 cudaError_t launch_b1(const LaunchArgs &a) {
   const GemvSegment one = {a.w, a.logits, a.n_rows, a.scale, a.cap};
-  SegTable T = make_table(&one, 1);
+  SegTable T = make_table(&one, 1, a.num_sms, true);
   T.argmax_precap = a.argmax_precap ? 1 : 0;
   float2 *parts = a.lse_parts ? a.ws.lse_parts : nullptr;   // batch row 0: one pair per CTA
   const int nb = a.k / kBlockWeights;
@@ -790,7 +861,7 @@ cudaError_t launch_b1(const LaunchArgs &a) {
 cudaError_t launch_b1_group(const float *hidden, const float *gamma, float eps, int k, const GemvSegment *segs,
                             int n, uint32_t *status, int num_sms, cudaStream_t stream, bool q4) {
   if (n < 1 || n > kMaxSegments) return cudaErrorInvalidValue;
-  const SegTable T = make_table(segs, n);
+  const SegTable T = make_table(segs, n, num_sms, true);
   if (q4) {
     switch (k / kBlockWeights) {
       case 26: return launch_b1_nb<26, true, true>(hidden, gamma, eps, T, nullptr, nullptr, nullptr, status,
