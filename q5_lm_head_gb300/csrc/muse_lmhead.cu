@@ -292,8 +292,10 @@ int muse_lmhead_forward_logprobs(muse_lmhead *h, const float *hidden, int batch,
   if (!g.ok) return MUSE_ERR_DEVICE;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the batch-1 kernel leaves one (max, sum exp) pair per CTA; other paths get a pass over the logits
-  // (the split-K kernel too: which CTA finishes a row varies, the pass keeps the sum's order fixed)
-  const bool fused = choose_path(h, batch) == Path::B1;
+  // (the split-K kernel too: which CTA finishes a row varies, the pass keeps the sum's order fixed).
+  // The pairs' buffer holds kMaxLseParts per batch row: a grid wider than that (a device with more
+  // SMs than the buffer has slots) takes the separate pass as well.
+  const bool fused = choose_path(h, batch) == Path::B1 && muse::b1_grid(h->n_rows, h->num_sms) <= muse::kMaxLseParts;
   st = run_forward(h, hidden, batch, gamma, eps, weights, scale, cap, logprobs, argmax, s, fused);
   if (st != MUSE_OK) return st;
   int n_parts;
