@@ -487,8 +487,13 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
       finish(j);
     }
     if (aborted && lane == 0) {
-      // never leave the CTA with copies in flight: wait (bounded) for the fills armed last
-      for (int j = first; j < issued; j += 2)
+      // Never leave the CTA with copies in flight: wait (bounded) for the fills
+      // of this producer's parity armed last, by it or, before the CTA-wide
+      // barrier, by the barrier thread (tiles below min(kEarly, my_tiles)).
+      int armed_end = issued;
+      const int early = kEarly < my_tiles ? kEarly : my_tiles;
+      while (armed_end < early) armed_end += 2;
+      for (int j = armed_end - C::kStages > pw ? armed_end - C::kStages : pw; j < armed_end; j += 2)
         ptx::mbar_wait(&full[j % C::kStages], static_cast<uint32_t>((j / C::kStages) & 1));
     }
     for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
