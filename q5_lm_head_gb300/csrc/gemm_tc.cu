@@ -334,6 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned long long *s_keys = reinterpret_cast<unsigned long long *>(mma_idle + 3);   // [32]
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(s_keys + 32);
   volatile uint32_t *s_abort = s_tmem + 1;
+  // [2]: the first chunk of both warpgroups of pair j is in tensor memory (16
+  // and 32 slots: the MMA warp starts on those K-steps while the second
+  // chunks are built, which takes the longer MMAs of wide batches partly off
+  // the pair's chain)
+  uint64_t *ahalf = reinterpret_cast<uint64_t *>(s_tmem + 2);
+  constexpr bool kEarlyHalf = NM >= 16;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t n_tiles = (n_rows + kTileRows - 1) / kTileRows;
@@ -374,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < 2; ++j) {
       ptx::mbar_init(&aready[j], 8);
       ptx::mbar_init(&adone[j], 1);
+      ptx::mbar_init(&ahalf[j], 8);
     }
     ptx::mbar_init(mma_idle, 1);
     ptx::mbar_init(xch_full, 32 * kUnpackWarps / 2);
@@ -448,22 +455,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int xs = 0;
     uint32_t xph = 0;
+    // 16 and 32 slots: one lane, elected once, issues and commits every MMA
+    bool issuer = false;
+    if constexpr (kEarlyHalf) issuer = tc::elect_one();
     for (int64_t g = 0; g < total; ++g) {
       if (__any_sync(0xffffffffu, *s_abort != 0u)) break;
       const int j = static_cast<int>(g & 1);
+      const uint32_t par = static_cast<uint32_t>((g >> 1) & 1);
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(&xfull[xs], xph));
-      if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(&aready[j], static_cast<uint32_t>((g >> 1) & 1)));
+      if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(kEarlyHalf ? &ahalf[j] : &aready[j], par));
       if (!ok) break;
       tc::fence_after();
       const uint32_t xbase = ptx::smem_u32(xst + xs * C::kPkgBytes);
       const uint64_t bdesc0 = tc::smem_desc_kmajor(xbase, C::kXRows * 16, 128);
       const uint64_t mdesc = tc::smem_desc_kmajor(xbase + C::kXBytes, min_rows<NM>() * 16, 128);
-      if (tc::elect_one()) {
-        const uint32_t d = tbase + C::col_d(j);
-        const uint32_t a = tbase + C::col_a(j);
+      const uint32_t d = tbase + C::col_d(j);
+      const uint32_t a = tbase + C::col_a(j);
+      // K-step ks: 16 columns of x = 2 core matrices along K
+      auto mma_ks = [&](int ks, bool acc) {
+        tc::mma_f16_tmemA(d, a + 8 * ks, bdesc0 + ((ks * 2 * (C::kXRows / 8) * 128) >> 4), C::kIdesc, acc);
+      };
+      if constexpr (kEarlyHalf) {
+        // the first chunks of both warpgroups (K-steps 0-3 and 8-11), then,
+        // once the whole A is in, the second chunks and the mins
+        if (issuer) {
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks)   // K-step ks: 16 columns of x = 2 core matrices along K
-          tc::mma_f16_tmemA(d, a + 8 * ks, bdesc0 + ((ks * 2 * (C::kXRows / 8) * 128) >> 4), C::kIdesc, ks > 0);
+          for (int ks = 0; ks < 4; ++ks) mma_ks(ks, ks > 0);
+#pragma unroll
+          for (int ks = 8; ks < 12; ++ks) mma_ks(ks, true);
+        }
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&aready[j], par))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        if (issuer) {
+#pragma unroll
+          for (int ks = 4; ks < 8; ++ks) mma_ks(ks, true);
+#pragma unroll
+          for (int ks = 12; ks < 16; ++ks) mma_ks(ks, true);
+          tc::mma_f16_tmemA(tbase + C::col_dmin(j), tbase + C::col_amin(j), mdesc, C::kIdescMin, false);
+          tc::commit(&adone[j]);
+          tc::commit(&xempty[xs]);
+        }
+      } else if (tc::elect_one()) {
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) mma_ks(ks, ks > 0);
         tc::mma_f16_tmemA(tbase + C::col_dmin(j), tbase + C::col_amin(j), mdesc, C::kIdescMin, false);
         tc::commit(&adone[j]);
         tc::commit(&xempty[xs]);
@@ -473,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) fail();
     // tensor memory is freed below only after every MMA issued here completed
-    if (tc::elect_one()) tc::commit(mma_idle);
+    if (kEarlyHalf ? issuer : tc::elect_one()) tc::commit(mma_idle);
     __syncwarp();
     if (!__all_sync(0xffffffffu, ptx::mbar_wait(mma_idle, 0)) && lane == 0) fail();
   } else {
@@ -653,7 +691,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      if (hf == 0) {
+      if constexpr (kEarlyHalf) {
+        if (hf == 0) a_chunk_st<kQ4, 0>(blk, chunk_consts<0>(hd.sc03), ta);
+        else a_chunk_st<kQ4, 2>(blk, chunk_consts<0>(hd.sc47), ta);
+        tc::wait_st();                               // K-steps 0-3 and 8-11 are ready
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ahalf[p]);
+        if (hf == 0) a_chunk_st<kQ4, 1>(blk, chunk_consts<2>(hd.sc03), ta + 32);
+        else a_chunk_st<kQ4, 3>(blk, chunk_consts<2>(hd.sc47), ta + 32);
+      } else if (hf == 0) {
         a_chunk_st<kQ4, 0>(blk, chunk_consts<0>(hd.sc03), ta);
         a_chunk_st<kQ4, 1>(blk, chunk_consts<2>(hd.sc03), ta + 32);
       } else {
