@@ -130,6 +130,9 @@ CASES = [
     (4096, 4096, 1, True, 20.0, True),
     (4099, 6656, 1, True, 20.0, True),      # ragged tail of the 12-row tiles
     (1000, 6656, 1, False, 0.0, False),
+    (153, 6656, 1, True, 20.0, True),       # even row shares: one row per CTA, two on the first
+    (1825, 6656, 1, True, 20.0, True),      # shares of 12 and 13 rows: a full tile and a one-row tile
+    (2000, 4096, 1, False, 0.0, False),     # shares on the 16-block build
     (4096, 6656, 5, True, 20.0, True),
     (777, 1024, 32, True, 20.0, True),
     (64, 4096, 16, True, 30.0, True),
