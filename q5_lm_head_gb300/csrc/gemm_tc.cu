@@ -51,7 +51,15 @@
 //      elected lane issues): per block, 16 K-steps of f16 MMAs with f32
 //      accumulation into D (M = 128, N = 2*NM: the x_hi and x_lo rows side by
 //      side) and one MMA A_min x x_min into Dmin; tcgen05.commit hands the
-//      buffer back.
+//      buffer back.  With 16 and 32 slots (N = 32, 64) it issues the K-steps
+//      of both warpgroups' first 64-column chunks as soon as those are in
+//      tensor memory, and the rest once the whole A is: the longer MMAs then
+//      overlap the second chunks' unpack instead of sitting in the pair's
+//      chain.
+//    * The weight tensor map promotes L2 fetches to 64 bytes: a 176-byte box
+//      row shares its first and last 256-byte line with the neighbouring
+//      boxes, whose bytes were often evicted (evict-first) before the
+//      neighbour came for them.
 #include <atomic>
 #include <cuda.h>
 #include <cudaTypedefs.h>
