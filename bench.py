@@ -615,25 +615,36 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    wall_ms = None
+    if flush is None:
+        # the timed steps: K forwards back to back behind a sleep kernel that
+        # holds the GPU while the host enqueues them (no interval waits on the
+        # host), two events around the whole run and none in between
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(_hold_cycles(args.steps))
+            t_begin.record(stream)
+            for _ in range(args.steps):
+                fwd()
+            t_end.record(stream)
+        torch.cuda.synchronize()
+        wall_ms = t_begin.elapsed_time(t_end)
     with torch.cuda.stream(stream):
-        # hold the GPU while the host enqueues every timed step, so that no
-        # interval below waits on the host
+        # per-forward device times (the kernel-only rate of the roofline; with
+        # a flush, the timed steps themselves): an event pair around each
+        # forward, L2 flushed before it when the inputs fit in L2
         torch.cuda._sleep(_hold_cycles(args.steps))
-        t_begin.record(stream)
         for i in range(args.steps):
             if flush is not None:
                 l2_flush(i)
             starts[i].record(stream)
             fwd()
             ends[i].record(stream)
-        t_end.record(stream)
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]     # ms, each forward
     kern_ms = sum(per) / len(per)
-    wall_ms = t_begin.elapsed_time(t_end)
     step_ms = statistics.median(per) if flush is not None else wall_ms / args.steps
 
     # small workloads: the same forward replayed from a CUDA graph (launch cost off the host path)
