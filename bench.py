@@ -458,6 +458,23 @@ def _time_forwards(fwd, stream, n, l2_flush=None):
     return [a.elapsed_time(b) for a, b in zip(starts, ends)]
 
 
+def _time_back_to_back(fwd, stream, n):
+    """Device time (ms) per forward of n forwards enqueued back to back
+    behind a sleep kernel, with one event before the first and one after the
+    last (none in between)."""
+    import torch
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(_hold_cycles(n, 0.1e-3, 1.0))
+        t0.record(stream)
+        for _ in range(n):
+            fwd()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / n
+
+
 def run_sweep(args, dev, stream, local, peak, peak_kind, preset=None):
     """Every workload of the metric on this GPU, one entry each: device time
     per forward (CUDA events; inputs larger than L2, or L2 flushed before
@@ -523,18 +540,24 @@ def run_sweep(args, dev, stream, local, peak, peak_kind, preset=None):
         sampler = ClockSampler(local)
         sampler.start()
         time.sleep(0.3)
+        wall_ms = _time_back_to_back(fwd, stream, n) if big else None
         per = _time_forwards(fwd, stream, n, None if big else l2_flush)
         clocks = sampler.stop()
-        ms = (sum(per) / len(per)) if big else statistics.median(per)
+        kern_ms = (sum(per) / len(per)) if big else statistics.median(per)
+        ms = wall_ms if big else kern_ms
         nbytes = wl.algorithmic_bytes()
         gbs = nbytes / (ms * 1e-3) / 1e9
         entries.append({
             "workload": name, "what": what, "batch": wl.batch, "n_rows": wl.n_rows, "k": wl.k,
             "weights": "Q5_K" if wl.fmt == "q5_k" else "Q4_K", "kernel_path": path, "forwards": n,
             "us_per_forward": round(ms * 1e3, 2),
-            "us_stat": "mean of per-forward CUDA-event intervals" if big else
+            "us_stat": "forwards back to back, two events around the run / forwards" if big else
                        "median of per-forward CUDA-event intervals, L2 flushed before each",
-            "algorithmic_bytes": nbytes, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "kernel_us": round(kern_ms * 1e3, 2),
+            "kernel_us_stat": "mean of per-forward CUDA-event intervals" if big else
+                              "median of per-forward CUDA-event intervals, L2 flushed before each",
+            "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
+            "frac_of_peak": round(nbytes / (kern_ms * 1e-3) / 1e9 / peak, 4),
             "logits_per_s": round(wl.batch * wl.n_rows / (ms * 1e-3), 1),
             "traffic": _profiled_traffic(path, name), "clocks": clocks, "device_status": head.device_status()})
         head.close()
