@@ -36,17 +36,21 @@
 //     copies (cp.async.bulk + mbarrier transaction counts, L2 evict-first);
 //     producer p owns the stages of parity p, so two copies are always being
 //     armed independently.  CTAs take tiles round-robin, so the whole GPU
-//     streams one contiguous stretch.  Each time consumers release one of its
+//     streams one contiguous stretch; a small single matrix, where the CTA with
+//     the most rows sets the time, is instead cut into even shares of rows
+//     (12-row tiles and one shorter one per CTA).  The arming thread writes each
+//     stage's row count for the consumers.  Each time consumers release one of its
 //     stages, a producer first re-arms it with its next tile and then finishes
 //     the released stage's rows: fixed-order sum of the block partials, scale +
 //     soft cap, store, argmax key.  The partial ring has two slots more than
 //     the stage ring, so a slot is never rewritten before its producer has read
 //     it (the rewrite needs a stage that the same producer arms only
 //     afterwards).
-//   * prologue: the thread that initialises the barriers bulk-copies the
-//     hidden row (and gamma) into the last stage (gamma into the one before
-//     when both do not fit) and then arms the first weight tiles of the other
-//     stages itself, before the CTA-wide barrier; the producers arm the rest.
+//   * prologue: thread 0 bulk-copies the hidden row (and gamma) into the last
+//     stage (gamma into the one before when both do not fit) before anything
+//     else, then initialises the other barriers and arms the first weight
+//     tiles of the other stages itself, before the CTA-wide barrier; the
+//     producers arm the rest.
 //     The consumers build the RMS factor and their activation planes from
 //     shared memory (the four threads of a unit each quantise a quarter of its
 //     64 columns and share the plane words through the same stage), then
