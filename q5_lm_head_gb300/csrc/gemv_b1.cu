@@ -309,6 +309,13 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  // Programmatic dependent launch: nothing of the previous launch's memory is
+  // touched before it has completed, and the next launch in the stream may
+  // start its CTAs as this launch's CTAs leave their SMs (one CTA fills an SM,
+  // so they cannot share one).  Not with the (max, sum exp) pairs: the small
+  // normaliser kernel that follows would then sit on the SMs beside this one.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (lse_parts == nullptr) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // This CTA's tiles: tile_first, tile_first + tile_step, ... of its chunk
   // (one chunk, all CTAs, unless split along K).  32-bit arithmetic: the grid
   // is at most the SM count and a tile count fits easily.
@@ -754,9 +761,18 @@ cudaError_t launch_b1_nb(const float *hidden, const float *gamma, float eps, con
   const int64_t units = n_tiles * n_chunks;
   const int64_t grid = kSplit ? (units < num_sms ? units : num_sms) : T.grid;
   if (kSplit && (n_chunks < 2 || grid < n_chunks || !split_part || !split_cnt)) return cudaErrorInvalidValue;
-  gemv_b1_kernel<NB, kGroup, kQ4, kSplit><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
-      hidden, gamma, eps, T, keys, ticket, argmax, status, lse_parts, n_chunks, split_part, split_cnt);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_b1_kernel<NB, kGroup, kQ4, kSplit>, hidden, gamma, eps, T, keys, ticket,
+                            argmax, status, lse_parts, n_chunks, split_part, split_cnt);
 }
 
 // The matrices' tile table and how the CTAs share the tiles.  Round-robin
