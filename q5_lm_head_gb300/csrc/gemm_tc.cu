@@ -133,8 +133,13 @@ __global__ void __launch_bounds__(kPrepThreads)
                   uint8_t *__restrict__ pkgs) {
   using C = TcCfg<NM>;
   __shared__ float s_part[kPrepThreads / 32];
-  // let the dependent GEMM start its set-up and weight stream now; it reads the
-  // packages only after this grid has completed
+  // A programmatic dependent of the previous forward's GEMM (which triggers
+  // near its end): nothing is read or written before that grid has completed,
+  // so this grid's launch overlaps its tail.  Then let the dependent GEMM
+  // start its set-up and weight stream; it reads the packages only after this
+  // grid has completed, and the writes it shares with the previous GEMM
+  // (logits, argmax keys, shared-tile counters) follow from those packages.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int kb = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -747,6 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  // the next forward's prep kernel may launch now (it waits for this grid)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == kMmaWarp) {
     tc::fence_after();
     tc::dealloc(tbase, kTmemCols);
@@ -788,10 +795,19 @@ cudaError_t launch_tc_nm(const LaunchArgs &a, const CUtensorMap &map) {
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   const int nb = a.k / kBlockWeights;
-  prep_x_kernel<NM><<<dim3(nb, min_rows<NM>()), kPrepThreads, 0, a.stream>>>(a.hidden, a.gamma, a.eps, a.batch,
-                                                                             a.k, a.ws.xpkg);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  {
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3(nb, min_rows<NM>());
+    pc.blockDim = dim3(kPrepThreads);
+    pc.stream = a.stream;
+    cudaLaunchAttribute pa[1];
+    pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // may start before the previous grid ends
+    pa[0].val.programmaticStreamSerializationAllowed = 1;
+    pc.attrs = pa;
+    pc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&pc, prep_x_kernel<NM>, a.hidden, a.gamma, a.eps, a.batch, a.k, a.ws.xpkg);
+    if (e != cudaSuccess) return e;
+  }
   const int64_t n_tiles = (a.n_rows + kTileRows - 1) / kTileRows;
   const int64_t pairs = n_tiles * (nb / 2);   // a narrow matrix spreads its step pairs over the SMs
   const int64_t grid = kNarrow ? (pairs < a.num_sms ? pairs : a.num_sms) : (n_tiles < a.num_sms ? n_tiles : a.num_sms);
