@@ -20,6 +20,19 @@
 // partials added in chunk order (the same bits whichever CTA that is), then
 // scale, cap and argmax.  No CTA waits on another.
 //
+// A Q4_K matrix of at most three chunks with few rows (an even share over the
+// SMs is at most eight tiles per CTA, the FFN down projection's shape) has no
+// hand-off at all: the K loop.  Each CTA takes an even share of rows and
+// streams all chunks of them, chunk after chunk (its tiles, rounded up to an
+// even count with an empty tile, for chunk 0, then for chunk 1, ...).  The
+// whole input row is staged once (in the last stage and the later chunks'
+// plane slots, so that only one stage waits for the prologue); the consumers
+// quantise all chunks in one pass (one RMS factor for the row), keep chunk 0's
+// planes in registers and the later chunks' plane words, step and column sums
+// in shared memory, and load a chunk's as its first tile comes up.  A producer keeps the
+// chunk sums of its rows in registers (tile t of every chunk is its tile),
+// adds them in chunk order and finishes a row with the last chunk.
+//
 // The argmax ranks the returned logit, or (argmax_precap) scale * raw before
 // the cap; the two orders agree except where the f32 cap rounds distinct
 // values to the same float.
@@ -84,8 +97,13 @@ constexpr int kStreams = 4;         // row teams of consumer threads
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // opt-in limit minus static shared memory
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 
+// K loop inside the CTA (kKLoop): a K of up to kMaxKLoopChunks chunks of NB
+// blocks, every CTA streaming all chunks of its own rows, chunk after chunk.
+constexpr int kMaxKLoopChunks = 3;
+constexpr int kMaxKLoopTiles = 8;      // tiles of a CTA's rows (even), so its row sums fit in registers
+
 // NB blocks per row; kQ4: Q4_K blocks (144 bytes, nibbles only) instead of Q5_K.
-template <int NB, bool kQ4>
+template <int NB, bool kQ4, bool kKLoop = false>
 struct B1Cfg {
   static constexpr int kUnits = 4 * NB;                    // (block, 64-column group) units per row
   static constexpr int kConsumers = kUnits * kStreams;
@@ -100,24 +118,42 @@ struct B1Cfg {
   static constexpr int kStageBytes = kRows * kRowBytes;
   static constexpr int kSlotBytes = kRows * NB * 4;         // one partial per (row, block)
   static constexpr int kFixedBytes = 640;                   // barriers, scratch, tile table, stage row counts
+  // (max, sum) of every quarter in the prologue; with the K loop (one table
+  // per chunk) chunk 0's is at the end of the staging stage and the later
+  // chunks' in the partial slots (unused until the first tile)
+  static constexpr int kExBytes = kKLoop ? 0 : kUnits * 4 * 8;
+  // K loop: the plane words, RMS-scaled step and column sums of chunks 1 and 2
+  // of every unit (chunk 0 stays in registers until its tiles are done)
+  static constexpr int kKPlaneStride = 52;                  // 48 plane words, sigma/2, two sums, pad
+  static constexpr int kPlanesBytes = kKLoop ? (kMaxKLoopChunks - 1) * kUnits * kKPlaneStride * 4 : 0;
   static constexpr int kStagesFit =
-      (kMaxSmem - kFixedBytes - 4 * 8 * kUnits - 2 * kSlotBytes) / (kStageBytes + kSlotBytes);
+      (kMaxSmem - kFixedBytes - kExBytes - kPlanesBytes - 2 * kSlotBytes) / (kStageBytes + kSlotBytes);
   static constexpr int kStages = (kStagesFit > 8 ? 8 : kStagesFit) & ~1;   // even: one parity per producer
   static_assert(kStages >= 4, "need at least double buffering per producer");
   static constexpr int kSlots = kStages + 2;
-  static constexpr int kExBytes = kUnits * 4 * 8;              // prologue: (max, sum) of every quarter
-  static constexpr int kSmemBytes = kStages * kStageBytes + kSlots * kSlotBytes + kFixedBytes + kExBytes;
+  static constexpr int kSmemBytes =
+      kStages * kStageBytes + kSlots * kSlotBytes + kFixedBytes + kExBytes + kPlanesBytes;
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
   // the prologue stages hidden (and gamma) in the last stage, or gamma in the one
-  // before when both do not fit one stage
+  // before when both do not fit one stage.  The K loop stages the whole hidden
+  // row (every chunk; gamma is read from global memory) in the last stage up
+  // to chunk 0's quarter table (kKStageRowBytes) and the rest in the plane
+  // slots, which are written only after the row has been read.
   static_assert(NB * kBlockWeights * 4 <= kStageBytes, "hidden fits one stage");
-  static constexpr int kHoldStages = 2 * NB * kBlockWeights * 4 <= kStageBytes ? 1 : 2;
+  static constexpr int kKStageRowBytes = kStageBytes - kUnits * 4 * 8;
+  static_assert(!kKLoop || (kKStageRowBytes >= NB * kBlockWeights * 4 && kKStageRowBytes % 64 == 0 &&
+                            kMaxKLoopChunks * NB * kBlockWeights * 4 <= kKStageRowBytes + kPlanesBytes),
+                "K loop: chunk 0 in the staging stage, the hidden row in the stage and the plane slots");
+  static_assert(kUnits * kKPlaneStride <= NB * kBlockWeights, "K loop: chunk 0's planes over its columns");
+  static constexpr int kHoldStages = !kKLoop && 2 * NB * kBlockWeights * 4 > kStageBytes ? 2 : 1;
   static constexpr int kEarlyTiles = kStages - kHoldStages;   // armed before the CTA-wide barrier
   // after the activations are loaded the staging stage holds, per unit, its
   // plane words (p2, p1, p0: 16 words each, padded to 52 so the units' rows
   // fall on distinct banks)
   static constexpr int kPlaneStride = 52;
   static_assert(kUnits * kPlaneStride * 4 <= kStageBytes, "plane area");
+  static_assert(!kKLoop || (kMaxKLoopChunks - 1) * kUnits * 4 * 8 <= kSlots * kSlotBytes,
+                "K loop: the later chunks' quarter tables fit the partial slots");
 };
 
 __device__ __forceinline__ uint32_t rotl32(uint32_t v, uint32_t s) { return __funnelshift_l(v, v, s); }
@@ -273,14 +309,15 @@ __device__ __forceinline__ TileLoc locate(const SegTable &T, int64_t tile) {
   return L;
 }
 
-template <int NB, bool kGroup, bool kQ4, bool kSplit>
-__global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
+template <int NB, bool kGroup, bool kQ4, bool kSplit, bool kKLoop>
+__global__ void __launch_bounds__(B1Cfg<NB, kQ4, kKLoop>::kThreads, 1)
     gemv_b1_kernel(const float *__restrict__ hidden, const float *__restrict__ gamma, float eps,
                    const __grid_constant__ SegTable segs, unsigned long long *keys, unsigned int *ticket,
                    int32_t *argmax, uint32_t *status, float2 *lse_parts, int n_chunks, float *split_part,
                    unsigned int *split_cnt) {
   static_assert(!(kSplit && kGroup), "a grouped launch is not split along K");
-  using C = B1Cfg<NB, kQ4>;
+  static_assert(!kKLoop || (kSplit && kQ4), "the K loop runs Q4_K launches split along K");
+  using C = B1Cfg<NB, kQ4, kKLoop>;
   constexpr int K = NB * kBlockWeights;                                    // columns of one chunk
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *stages = smem;
@@ -299,7 +336,11 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
   unsigned long long *s_best = reinterpret_cast<unsigned long long *>(s_red + 32);
   volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(s_best + 1);
   float2 *s_ms = reinterpret_cast<float2 *>(s_best + 2);                   // [2] producers' (max, sum exp)
-  float2 *s_ex = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(full) + C::kFixedBytes);   // [kUnits][4]
+  // [kUnits][4]; with the K loop chunk 0's at the end of the staging stage
+  float2 *s_ex = kKLoop ? reinterpret_cast<float2 *>(const_cast<float *>(s_hidden) + C::kKStageRowBytes / 4)
+                        : reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(full) + C::kFixedBytes);
+  // K loop: [chunk 1, 2][kUnits][kKPlaneStride] words
+  uint32_t *s_planes = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(full) + C::kFixedBytes + C::kExBytes);
   static_assert(16 * C::kStages + 176 <= 512, "fixed area: barriers and scratch");
   // rows of the tile in each stage, written by whoever arms the stage before its
   // expect-tx arrive (release) and read by the consumers after the stage's
@@ -320,7 +361,7 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
   // (one chunk, all CTAs, unless split along K).  32-bit arithmetic: the grid
   // is at most the SM count and a tile count fits easily.
   int chunk = 0, tile_first = static_cast<int>(blockIdx.x), tile_step = static_cast<int>(gridDim.x);
-  if constexpr (kSplit) {
+  if constexpr (kSplit && !kKLoop) {
     const int g = static_cast<int>(gridDim.x), bx = static_cast<int>(blockIdx.x);
     chunk = ((bx + 1) * n_chunks - 1) / g;
     const int lo = chunk * g / n_chunks;
@@ -335,9 +376,17 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     ptx::mbar_init(pro_full, 1);
     ptx::fence_barrier_init();
     const uint32_t row_bytes = static_cast<uint32_t>(K) * 4u;
-    ptx::mbar_arrive_expect_tx(pro_full, gamma ? 2u * row_bytes : row_bytes);
-    ptx::bulk_g2s_nohint(const_cast<float *>(s_hidden), x_src, row_bytes, pro_full);
-    if (gamma) ptx::bulk_g2s_nohint(const_cast<float *>(s_gamma), g_src, row_bytes, pro_full);
+    if constexpr (kKLoop) {                // every chunk of the row; gamma stays in global memory
+      const uint32_t total = static_cast<uint32_t>(n_chunks) * row_bytes;
+      const uint32_t first = total < C::kKStageRowBytes ? total : C::kKStageRowBytes;
+      ptx::mbar_arrive_expect_tx(pro_full, total);
+      ptx::bulk_g2s_nohint(const_cast<float *>(s_hidden), hidden, first, pro_full);
+      if (total > first) ptx::bulk_g2s_nohint(s_planes, hidden + first / 4, total - first, pro_full);
+    } else {
+      ptx::mbar_arrive_expect_tx(pro_full, gamma ? 2u * row_bytes : row_bytes);
+      ptx::bulk_g2s_nohint(const_cast<float *>(s_hidden), x_src, row_bytes, pro_full);
+      if (gamma) ptx::bulk_g2s_nohint(const_cast<float *>(s_gamma), g_src, row_bytes, pro_full);
+    }
   }
   const int n_tiles = static_cast<int>(segs.tile_end[segs.n - 1]);
   int my_tiles = tile_first < n_tiles ? (n_tiles - 1 - tile_first) / tile_step + 1 : 0;
@@ -346,25 +395,33 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
   const int b_first = bx * segs.rows_per + (bx < segs.extra ? bx : segs.extra);
   const int b_rows = segs.rows_per + (bx < segs.extra ? 1 : 0);
   if (segs.balanced) my_tiles = (b_rows + kRows - 1) / kRows;
+  // K loop: the CTA's tiles (rounded up to an even count, an empty tile
+  // padding an odd one, so that every chunk's tile t goes to producer t mod 2)
+  // for chunk 0, then for chunk 1, ...: local tile j is tile j mod kl_tiles of
+  // chunk j / kl_tiles
+  const int kl_tiles = my_tiles + (my_tiles & 1);
+  if constexpr (kKLoop) my_tiles = kl_tiles * n_chunks;
   // local tile j of this CTA: its matrix, first row and rows
   auto tile_at = [&](int j) -> TileLoc {
     if (segs.balanced) {
+      if constexpr (kKLoop) j %= kl_tiles;
       const int left = b_rows - j * kRows;
-      return TileLoc{0, b_first + j * kRows, left < kRows ? left : kRows};
+      return TileLoc{0, b_first + j * kRows, left <= 0 ? 0 : (left < kRows ? left : kRows)};
     }
     return locate<kGroup>(segs, tile_first + static_cast<int64_t>(j) * tile_step);
   };
   // weight tiles armed by the barrier thread before the CTA-wide barrier; a
   // split chunk's tiles are row-strided (one copy per row), so its producers
-  // arm them all, a row per lane
-  constexpr int kEarly = kSplit ? 0 : C::kEarlyTiles;
+  // arm them, a row per lane, but the K loop's first tile (which its consumers
+  // wait for first) goes out ahead of the others from the barrier thread
+  constexpr int kEarly = kKLoop ? 1 : kSplit ? 0 : C::kEarlyTiles;
   // the rows of local tile j: one bulk copy, or one per row of a split chunk
   // (rows n_chunks * kRowBytes apart); lanes l0, l0 + ls, ... issue them
-  auto issue_tile = [&](const TileLoc &L, int st, uint64_t policy, int l0, int ls) {
+  auto issue_tile = [&](const TileLoc &L, int st, uint64_t policy, int l0, int ls, int q) {
     uint8_t *dst = stages + st * C::kStageBytes;
     if constexpr (kSplit) {
       const int64_t stride = static_cast<int64_t>(n_chunks) * C::kRowBytes;
-      const uint8_t *src = segs.seg[0].w + L.r0 * stride + static_cast<int64_t>(chunk) * C::kRowBytes;
+      const uint8_t *src = segs.seg[0].w + L.r0 * stride + static_cast<int64_t>(q) * C::kRowBytes;
       for (int i = l0; i < L.rows; i += ls)
         ptx::bulk_g2s(dst + i * C::kRowBytes, src + i * stride, C::kRowBytes, &full[st], policy);
     } else if (l0 == 0) {
@@ -390,7 +447,7 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
       const TileLoc L = tile_at(j);
       s_rows[j] = L.rows;
       ptx::mbar_arrive_expect_tx(&full[j], static_cast<uint32_t>(L.rows * C::kRowBytes));
-      issue_tile(L, j, policy, 0, 1);
+      issue_tile(L, j, policy, 0, 1, kKLoop ? j / kl_tiles : chunk);
     }
   }
   __syncthreads();
@@ -412,6 +469,11 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
     const int er = lane >> 1, eq = lane & 1;
     unsigned long long best = 0ull;
     MaxSum ms = ms_empty();                     // log-softmax normaliser of this lane's rows
+    // K loop: the chunk sums so far of row er of this producer's tiles t = pw,
+    // pw + 2, ... (register k holds tile 2k + pw)
+    float racc[kMaxKLoopTiles / 2];
+#pragma unroll
+    for (int i = 0; i < kMaxKLoopTiles / 2; ++i) racc[i] = 0.0f;
     // finish the rows of local tile j (its consumers have released its stage)
     auto finish = [&](int j) {
       const TileLoc L = tile_at(j);
@@ -424,7 +486,22 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
           if (g + eq < NB) sacc += pr[g + eq];
       }
       sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
-      if constexpr (kSplit) {
+      if constexpr (kKLoop) {
+        // the chunk partials of a row added in chunk order, from zero; the
+        // rows are finished with the last chunk
+        const int q = j / kl_tiles, k2 = (j % kl_tiles) >> 1;
+        float prev = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kMaxKLoopTiles / 2; ++i)
+          if (i == k2) prev = racc[i];
+        sacc = (q == 0 ? 0.0f : prev) + sacc;
+        if (q < n_chunks - 1) {
+#pragma unroll
+          for (int i = 0; i < kMaxKLoopTiles / 2; ++i)
+            if (i == k2) racc[i] = sacc;
+          return;
+        }
+      } else if constexpr (kSplit) {
         // this chunk's row sums out (plain stores); the CTA counts the tile in
         // and finishes it after its last tile, off the copy-issue path
         if (eq == 0 && er < L.rows) split_part[static_cast<int64_t>(chunk) * G.n_rows + L.r0 + er] = sacc;
@@ -467,14 +544,16 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
         }
       }
       if constexpr (kSplit) {                  // every tile, one row per lane
-        const TileLoc L = tile_at(j);
-        const int st = j % C::kStages;
-        if (lane == 0) {
-          s_rows[st] = L.rows;
-          ptx::mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(L.rows * C::kRowBytes));
+        if (j >= kEarly) {
+          const TileLoc L = tile_at(j);
+          const int st = j % C::kStages;
+          if (lane == 0) {
+            s_rows[st] = L.rows;
+            ptx::mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(L.rows * C::kRowBytes));
+          }
+          __syncwarp();
+          issue_tile(L, st, policy, lane, 32, kKLoop ? j / kl_tiles : chunk);
         }
-        __syncwarp();
-        issue_tile(L, st, policy, lane, 32);
       } else if (lane == 0 && j >= C::kEarlyTiles) {   // the first ones went out with the barrier set-up
         const TileLoc L = tile_at(j);
         const uint32_t bytes = static_cast<uint32_t>(L.rows * C::kRowBytes);
@@ -521,21 +600,152 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
 
     // Prologue: the hidden row (and gamma) arrive in the last stage.  Unit u's
     // 64 columns are quantised by its four threads (one per stream), a quarter
-    // (16 columns) each: quarter q = (stream + u) mod 4, chunk order rotated by
-    // (u / 2) mod 4, which puts the eight lanes of every quarter-warp on
-    // distinct shared-memory banks.  The quantisation step is a power of two
-    // fixed by the largest |h * gamma| of the unit, so it needs neither the RMS
-    // factor r nor a division: r only scales sigma and the column sums.  Two
+    // (16 columns) each: quarter q = (stream + qoff(u mod 4)) mod 4 with qoff =
+    // 0, 1, 1, 2, its four 4-column pieces taken in an order rotated by
+    // ((u mod 8) / 2 + the lane's quarter-warp) mod 4.  That puts the eight
+    // lanes of every quarter-warp on distinct banks for the row's 16-byte
+    // loads, and the 32 lanes of a warp on distinct banks for each plane-word
+    // store (two ways where a warp spans two streams).  The quantisation step
+    // is a power of two fixed by the largest |h * gamma| of the unit, so it
+    // needs neither the RMS factor r nor a division: r only scales sigma and
+    // the column sums.  Two
     // barriers: after the first every consumer has read the staged row and
     // posted its sum of squares and its quarter's (max, sum); after the second
     // the unit's plane words are in shared memory.
-    bool pro_ok = __all_sync(0xffffffffu, ptx::mbar_wait(pro_full, 0));
-    if (!pro_ok && lane == 0) fail();
     XPlanes xl, xh;
     float sx_lo, sx_hi, sigma_half;
+    bool pro_ok;
+    if constexpr (kKLoop) {
+      // All chunks at once, each the same way as the one chunk below (a
+      // thread's quarters of all units tile the row once, so they also give
+      // the row's sum of squares: one RMS factor for all chunks).  Chunk 0's
+      // plane words are shared over its own (by then consumed) hidden columns
+      // and loaded into registers; the later chunks' plane words, sigma/2 and
+      // column sums go to their slots (over the rest of the consumed row) for
+      // the main loop.  The gamma quarters are loaded from global memory while
+      // the row is copied.
+      const int q = (stream + (((u & 3) + 1) >> 1)) & 3;
+      const int rot = (((u & 7) >> 1) + ((tid >> 3) & 3)) & 3;
+      const int base = kb * kBlockWeights + 64 * c + 16 * q;
+      float4 gv[kMaxKLoopChunks][4];
+#pragma unroll
+      for (int cc = 0; cc < kMaxKLoopChunks; ++cc)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          gv[cc][i] = gamma && cc < n_chunks
+                          ? __ldg(reinterpret_cast<const float4 *>(gamma + cc * K + base + 4 * ((i + rot) & 3)))
+                          : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+      pro_ok = __all_sync(0xffffffffu, ptx::mbar_wait(pro_full, 0));
+      if (!pro_ok && lane == 0) fail();
+      float xv[kMaxKLoopChunks][4][4];
+      float ss = 0.0f;
+#pragma unroll
+      for (int cc = 0; cc < kMaxKLoopChunks; ++cc) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int off = cc * K + base + 4 * ((i + rot) & 3);
+          float4 h = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          if (cc < n_chunks) {             // a quarter (64 bytes) never straddles the two parts
+            constexpr int kIn = C::kKStageRowBytes / 4;   // columns in the staging stage
+            h = *reinterpret_cast<const float4 *>(off < kIn ? s_hidden + off
+                                                            : reinterpret_cast<const float *>(s_planes) + (off - kIn));
+            if (gamma) {
+              const float4 g = gv[cc][i];
+              ss = fmaf(h.x, h.x, ss);
+              ss = fmaf(h.y, h.y, ss);
+              ss = fmaf(h.z, h.z, ss);
+              ss = fmaf(h.w, h.w, ss);
+              h = make_float4(h.x * g.x, h.y * g.y, h.z * g.z, h.w * g.w);
+            }
+          }
+          xv[cc][i][0] = h.x; xv[cc][i][1] = h.y; xv[cc][i][2] = h.z; xv[cc][i][3] = h.w;
+        }
+        if (cc < n_chunks) {
+          float amax = 0.0f, psum = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            psum += (xv[cc][i][0] + xv[cc][i][1]) + (xv[cc][i][2] + xv[cc][i][3]);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(xv[cc][i][0]), fabsf(xv[cc][i][1])),
+                                     fmaxf(fabsf(xv[cc][i][2]), fabsf(xv[cc][i][3]))));
+          }
+          float2 *ex = cc == 0 ? s_ex : reinterpret_cast<float2 *>(slots) + (cc - 1) * C::kUnits * 4;
+          ex[u * 4 + q] = make_float2(amax, psum);
+        }
+      }
+      if (gamma) {
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) s_red[warp] = ss;
+      }
+      ptx::named_bar_sync(1, C::kConsumers);
+      float r = 1.0f;
+      if (gamma) {                              // the warps' sums in warp order
+        float tot = 0.0f;
+        for (int i = 0; i < C::kConsumerWarps; ++i) tot += s_red[i];
+        r = rsqrtf(fmaf(tot, 1.0f / static_cast<float>(K * n_chunks), eps));
+      }
+#pragma unroll
+      for (int cc = 0; cc < kMaxKLoopChunks; ++cc) {
+        if (cc >= n_chunks) break;
+        const float2 *ex = cc == 0 ? s_ex : reinterpret_cast<const float2 *>(slots) + (cc - 1) * C::kUnits * 4;
+        const float4 e01 = *reinterpret_cast<const float4 *>(ex + u * 4);
+        const float4 e23 = *reinterpret_cast<const float4 *>(ex + u * 4 + 2);
+        const float umax = fmaxf(fmaxf(e01.x, e01.z), fmaxf(e23.x, e23.z));
+        const float slo = r * (e01.y + e01.w), shi = r * (e23.y + e23.w);
+        float inv = 0.0f, sh = 0.0f;
+        if (umax > 0.0f) {
+          const int eb = pow2_step_exponent(umax);
+          inv = __uint_as_float(static_cast<uint32_t>(eb) << 23);
+          sh = r * __uint_as_float(static_cast<uint32_t>(253 - eb) << 23);
+        }
+        uint32_t *s_pl = cc == 0 ? reinterpret_cast<uint32_t *>(const_cast<float *>(s_hidden)) + u * C::kKPlaneStride
+                                 : s_planes + ((cc - 1) * C::kUnits + u) * C::kKPlaneStride;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t w2, w1, w0;
+          quantize_chunk(xv[cc][i], inv, w2, w1, w0);
+          const int ch = 4 * q + ((i + rot) & 3);
+          s_pl[ch] = w2;
+          s_pl[16 + ch] = w1;
+          s_pl[32 + ch] = w0;
+        }
+        if (cc == 0) {
+          sx_lo = slo;
+          sx_hi = shi;
+          sigma_half = sh;
+        } else if (stream == 0) {
+          s_pl[48] = __float_as_uint(sh);
+          s_pl[49] = __float_as_uint(slo);
+          s_pl[50] = __float_as_uint(shi);
+        }
+      }
+      ptx::named_bar_sync(1, C::kConsumers);
+      const uint32_t *s_pl = reinterpret_cast<const uint32_t *>(s_hidden) + u * C::kKPlaneStride;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const uint4 a2 = *reinterpret_cast<const uint4 *>(s_pl + 4 * m);
+        const uint4 a1 = *reinterpret_cast<const uint4 *>(s_pl + 16 + 4 * m);
+        const uint4 a0 = *reinterpret_cast<const uint4 *>(s_pl + 32 + 4 * m);
+        const uint4 b2 = *reinterpret_cast<const uint4 *>(s_pl + 8 + 4 * m);
+        const uint4 b1 = *reinterpret_cast<const uint4 *>(s_pl + 24 + 4 * m);
+        const uint4 b0 = *reinterpret_cast<const uint4 *>(s_pl + 40 + 4 * m);
+        xl.p2[4 * m] = a2.x; xl.p2[4 * m + 1] = a2.y; xl.p2[4 * m + 2] = a2.z; xl.p2[4 * m + 3] = a2.w;
+        xl.p1[4 * m] = a1.x; xl.p1[4 * m + 1] = a1.y; xl.p1[4 * m + 2] = a1.z; xl.p1[4 * m + 3] = a1.w;
+        xl.p0[4 * m] = a0.x; xl.p0[4 * m + 1] = a0.y; xl.p0[4 * m + 2] = a0.z; xl.p0[4 * m + 3] = a0.w;
+        xh.p2[4 * m] = b2.x; xh.p2[4 * m + 1] = b2.y; xh.p2[4 * m + 2] = b2.z; xh.p2[4 * m + 3] = b2.w;
+        xh.p1[4 * m] = b1.x; xh.p1[4 * m + 1] = b1.y; xh.p1[4 * m + 2] = b1.z; xh.p1[4 * m + 3] = b1.w;
+        xh.p0[4 * m] = b0.x; xh.p0[4 * m + 1] = b0.y; xh.p0[4 * m + 2] = b0.z; xh.p0[4 * m + 3] = b0.w;
+      }
+      uint32_t dep = (xl.p2[0] ^ xl.p2[4]) ^ (xl.p1[0] ^ xl.p1[4]) ^ (xl.p0[0] ^ xl.p0[4]) ^
+                     (xh.p2[0] ^ xh.p2[4]) ^ (xh.p1[0] ^ xh.p1[4]) ^ (xh.p0[0] ^ xh.p0[4]);
+      asm volatile("mov.b32 %0, %0;" : "+r"(dep));
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(pro_done);
+    } else {
+    pro_ok = __all_sync(0xffffffffu, ptx::mbar_wait(pro_full, 0));
+    if (!pro_ok && lane == 0) fail();
     {
-      const int q = (stream + u) & 3;
-      const int rot = (u >> 1) & 3;
+      const int q = (stream + (((u & 3) + 1) >> 1)) & 3;
+      const int rot = (((u & 7) >> 1) + ((tid >> 3) & 3)) & 3;
       const int base = kb * kBlockWeights + 64 * c + 16 * q;
       float xv[4][4];
       float amax = 0.0f, psum = 0.0f, ss = 0.0f;
@@ -630,13 +840,42 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(pro_done);
     }
+    }
     const UnitSel us = make_unit_sel<kQ4>(c);
 
     int st = 0, ps = 0;
     uint32_t ph = 0;                           // round parity of the stage ring
+    int in_chunk = 0, kchunk = 0;              // K loop: tiles done of the current chunk
     for (int j = 0; j < my_tiles && pro_ok; ++j) {
       // every exit decision is taken by the whole warp (the loop body shuffles)
       if (__any_sync(0xffffffffu, *s_abort != 0u)) break;
+      if constexpr (kKLoop) {
+        if (in_chunk == kl_tiles) {            // the next chunk's activations
+          in_chunk = 0;
+          ++kchunk;
+          const uint32_t *s_pl = s_planes + ((kchunk - 1) * C::kUnits + u) * C::kKPlaneStride;
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const uint4 a2 = *reinterpret_cast<const uint4 *>(s_pl + 4 * m);
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(s_pl + 16 + 4 * m);
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(s_pl + 32 + 4 * m);
+            const uint4 b2 = *reinterpret_cast<const uint4 *>(s_pl + 8 + 4 * m);
+            const uint4 b1 = *reinterpret_cast<const uint4 *>(s_pl + 24 + 4 * m);
+            const uint4 b0 = *reinterpret_cast<const uint4 *>(s_pl + 40 + 4 * m);
+            xl.p2[4 * m] = a2.x; xl.p2[4 * m + 1] = a2.y; xl.p2[4 * m + 2] = a2.z; xl.p2[4 * m + 3] = a2.w;
+            xl.p1[4 * m] = a1.x; xl.p1[4 * m + 1] = a1.y; xl.p1[4 * m + 2] = a1.z; xl.p1[4 * m + 3] = a1.w;
+            xl.p0[4 * m] = a0.x; xl.p0[4 * m + 1] = a0.y; xl.p0[4 * m + 2] = a0.z; xl.p0[4 * m + 3] = a0.w;
+            xh.p2[4 * m] = b2.x; xh.p2[4 * m + 1] = b2.y; xh.p2[4 * m + 2] = b2.z; xh.p2[4 * m + 3] = b2.w;
+            xh.p1[4 * m] = b1.x; xh.p1[4 * m + 1] = b1.y; xh.p1[4 * m + 2] = b1.z; xh.p1[4 * m + 3] = b1.w;
+            xh.p0[4 * m] = b0.x; xh.p0[4 * m + 1] = b0.y; xh.p0[4 * m + 2] = b0.z; xh.p0[4 * m + 3] = b0.w;
+          }
+          const uint4 ex = *reinterpret_cast<const uint4 *>(s_pl + 48);
+          sigma_half = __uint_as_float(ex.x);
+          sx_lo = __uint_as_float(ex.y);
+          sx_hi = __uint_as_float(ex.z);
+        }
+        ++in_chunk;
+      }
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full[st], ph))) {
         if (lane == 0) fail();
         break;
@@ -673,7 +912,7 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
   }
 
   __syncthreads();
-  if constexpr (kSplit) {
+  if constexpr (kSplit && !kKLoop) {
     // Count this CTA's tiles in, a thread per tile; the tiles it arrived last on
     // are finished by the whole CTA, a (tile, row) job per thread: the chunk
     // partials added in chunk order, then scale, cap, store and argmax key.
@@ -739,28 +978,34 @@ __global__ void __launch_bounds__(B1Cfg<NB, kQ4>::kThreads, 1)
   if (argmax) argmax_publish_finish(keys, ticket, argmax, s_best, 1);
 }
 
-template <int NB, bool kGroup, bool kQ4, bool kSplit = false>
+template <int NB, bool kGroup, bool kQ4, bool kSplit = false, bool kKLoop = false>
 cudaError_t launch_b1_nb(const float *hidden, const float *gamma, float eps, const SegTable &T,
                          unsigned long long *keys, unsigned int *ticket, int32_t *argmax, uint32_t *status,
                          float2 *lse_parts, int num_sms, cudaStream_t stream, int n_chunks = 1,
                          float *split_part = nullptr, unsigned int *split_cnt = nullptr) {
-  using C = B1Cfg<NB, kQ4>;
+  using C = B1Cfg<NB, kQ4, kKLoop>;
   static std::atomic<unsigned long long> configured{0};   // one bit per device: the attribute is per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(gemv_b1_kernel<NB, kGroup, kQ4, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+    e = cudaFuncSetAttribute(gemv_b1_kernel<NB, kGroup, kQ4, kSplit, kKLoop>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   const int64_t n_tiles = T.tile_end[T.n - 1];
   // split along K: n_chunks row tiles per tile of rows, at least one CTA per chunk
   const int64_t units = n_tiles * n_chunks;
-  const int64_t grid = kSplit ? (units < num_sms ? units : num_sms) : T.grid;
-  if (kSplit && (n_chunks < 2 || grid < n_chunks || !split_part || !split_cnt)) return cudaErrorInvalidValue;
+  const int64_t grid = kSplit && !kKLoop ? (units < num_sms ? units : num_sms) : T.grid;
+  if (kKLoop) {   // balanced shares of at most kMaxKLoopTiles tiles, every chunk in every CTA
+    const int share = T.rows_per + (T.extra ? 1 : 0);
+    if (n_chunks < 2 || n_chunks > kMaxKLoopChunks || !T.balanced || share > kMaxKLoopTiles * kRows)
+      return cudaErrorInvalidValue;
+  } else if (kSplit && (n_chunks < 2 || grid < n_chunks || !split_part || !split_cnt)) {
+    return cudaErrorInvalidValue;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(C::kThreads);
@@ -771,8 +1016,8 @@ cudaError_t launch_b1_nb(const float *hidden, const float *gamma, float eps, con
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_b1_kernel<NB, kGroup, kQ4, kSplit>, hidden, gamma, eps, T, keys, ticket,
-                            argmax, status, lse_parts, n_chunks, split_part, split_cnt);
+  return cudaLaunchKernelEx(&cfg, gemv_b1_kernel<NB, kGroup, kQ4, kSplit, kKLoop>, hidden, gamma, eps, T, keys,
+                            ticket, argmax, status, lse_parts, n_chunks, split_part, split_cnt);
 }
 
 // The matrices' tile table and how the CTAs share the tiles.  Round-robin
@@ -837,11 +1082,29 @@ cudaError_t launch_b1_split(const LaunchArgs &a) {
   split_shape(a.k, cnb, s);
   if (b1_split_chunks(a.k) == 0 || a.num_sms < s) return cudaErrorInvalidValue;
   const GemvSegment one = {a.w, a.logits, a.n_rows, a.scale, a.cap};
-  SegTable T = make_table(&one, 1, a.num_sms, false);
-  T.argmax_precap = a.argmax_precap ? 1 : 0;
   // no (max, sum exp) pairs: which CTA finishes a row varies from run to run,
   // so the logprobs take the separate pass over the logits (fixed order)
   float2 *parts = nullptr;
+  // A Q4_K matrix of up to kMaxKLoopChunks chunks whose rows, shared evenly
+  // over the SMs, give every CTA at most kMaxKLoopTiles tiles: each CTA runs
+  // all chunks of its own rows (no partials through global memory).
+  const int64_t kl_grid = a.n_rows < a.num_sms ? a.n_rows : a.num_sms;
+  if (a.q4 && s <= kMaxKLoopChunks && a.n_rows > 0 &&
+      (a.n_rows + kl_grid - 1) / kl_grid <= static_cast<int64_t>(kMaxKLoopTiles) * kRows) {
+    SegTable T = make_table(&one, 1, a.num_sms, false);
+    T.balanced = 1;
+    T.grid = static_cast<int>(kl_grid);
+    T.rows_per = static_cast<int>(a.n_rows / kl_grid);
+    T.extra = static_cast<int>(a.n_rows % kl_grid);
+    T.argmax_precap = a.argmax_precap ? 1 : 0;
+    if (cnb == 26)
+      return launch_b1_nb<26, false, true, true, true>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
+                                                       a.ws.status, parts, a.num_sms, a.stream, s);
+    return launch_b1_nb<16, false, true, true, true>(a.hidden, a.gamma, a.eps, T, a.ws.keys, a.ws.ticket, a.argmax,
+                                                     a.ws.status, parts, a.num_sms, a.stream, s);
+  }
+  SegTable T = make_table(&one, 1, a.num_sms, false);
+  T.argmax_precap = a.argmax_precap ? 1 : 0;
   float *part = a.ws.b1_part;
   unsigned int *cnt = a.ws.b1_cnt;
   if (cnb == 26)

@@ -8,6 +8,11 @@ cap and argmax ("Chapter 20 — Final norm, LM head, and the soft cap": §20.1
 the computation, §20.3 the block format).  The RMS factor of the final norm
 covers the whole row, all chunks.
 
+A Q4_K matrix of at most three chunks whose rows, shared evenly over the SMs,
+give every CTA at most eight 12-row tiles runs the chunks inside each CTA
+instead (the K loop): a CTA streams all chunks of its own rows, one after the
+other, and adds the chunk sums of a row in chunk order in registers.
+
 Bar as everywhere: |gpu - oracle| <= 2e-3 on every logit (after the cap, raw
 with it off); the argmax equal to the oracle's where its top-2 gap exceeds
 4e-3.  Also: logprobs, repeated forwards bit for bit (whichever CTA finishes a
@@ -68,6 +73,14 @@ SHAPES = [
     (777, 13312, "q4_k", True, 20.0),
     (130, 32768, "q4_k", False, 0.0),       # 8 chunks of 4,096
     (50, 65536, "q5_k", True, 20.0),        # 16 chunks of 4,096: the most the split build takes
+    # the K loop (Q4_K, at most 3 chunks, at most 96 rows per CTA)
+    (6656, 19968, "q4_k", True, 20.0),      # the FFN down shape: 44 rows per CTA, 3 chunks of 6,656
+    (6656, 19968, "q4_k", False, 0.0),
+    (2000, 12288, "q4_k", True, 20.0),      # 3 chunks of 4,096
+    (1, 19968, "q4_k", True, 20.0),         # one row, one CTA
+    (153, 19968, "q4_k", True, 20.0),       # one CTA with two rows, the others one
+    (14592, 8192, "q4_k", True, 20.0),      # 96 rows per CTA: the most the K loop takes
+    (14593, 8192, "q4_k", True, 20.0),      # one row more: the cross-CTA hand-off
 ]
 
 
@@ -152,6 +165,33 @@ def test_split_k_after_clear_device_status(torch_cuda):
         assert head.device_status() == 0
     ref = oracle.lmhead(hidden, gamma, wq, synth.LOGIT_SCALE, synth.SOFTCAP, synth.RMS_EPS)
     _check(logits.cpu().numpy(), am.cpu().numpy(), ref, "after clear")
+
+
+def test_k_loop_repeats_and_logprobs(torch_cuda):
+    """The K loop: the same bits from forward to forward with alternating
+    inputs, and logprobs from the separate pass over its logits."""
+    import q5_lm_head_gb300 as mlh
+    torch = torch_cuda
+    n, k = 6656, 19968
+    hidden, gamma, wq = _inputs(n, k, True, "q4_k", 25)
+    with mlh.LMHead(n, k, max_batch=1, device=0, fmt="q4_k") as head:
+        assert head.path_name(1) == "gemv_b1_split"
+        h1, h2 = _dev(torch, hidden), _dev(torch, hidden[:, ::-1].copy())
+        w, g = _dev(torch, wq), _dev(torch, gamma)
+        outs = [[t.clone() for t in head.forward(h, w, g)] for h in (h1, h2, h1, h2, h1)]
+        lp, lse, am = head.forward_logprobs(h1, w, g, synth.RMS_EPS, synth.LOGIT_SCALE, synth.SOFTCAP, True)
+        torch.cuda.synchronize()
+        assert head.device_status() == 0
+        lp, lse, am = (t.cpu().numpy() for t in (lp, lse, am))
+    for i in (2, 4):
+        assert torch.equal(outs[0][0], outs[i][0]) and torch.equal(outs[0][1], outs[i][1])
+    assert torch.equal(outs[1][0], outs[3][0])
+    ref = oracle.lmhead(hidden, gamma, wq, synth.LOGIT_SCALE, synth.SOFTCAP, synth.RMS_EPS, fmt="q4_k")
+    _check(outs[0][0].cpu().numpy(), outs[0][1].cpu().numpy(), ref, "k loop")
+    ref_lp, ref_lse = oracle.log_softmax(ref)
+    assert np.abs(lp.astype(np.float64) - ref_lp).max() <= TOL
+    assert np.abs(lse.astype(np.float64) - ref_lse).max() <= TOL
+    assert am[0] == int(outs[0][1].cpu().numpy()[0])
 
 
 @pytest.mark.parametrize("n,k,b,path", [
